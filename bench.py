@@ -1,0 +1,414 @@
+"""Benchmark of the SP-TP FFN boundary on GB300.
+
+One step = one pass of the whole boundary (partial sum + residual + RMSNorm,
+chunked gate/up GEMM + SwiGLU, down GEMM) over one batch of synthetic input,
+at M=8192 tokens, d=4096, F=14336, P=2 shards, 8 sequence chunks, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N>1 runs under torch.distributed.run: every rank runs an independent replica
+of the workload on its own GPU (weak scaling, no data-path collective); the
+barrier and the max-over-ranks of the timed region use the process group.
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SP-TP FFN forward TFLOP/s & tokens/s (d=4096, M=8192, bf16), % of roofline"
+UNIT = "TFLOP/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload():
+    from sequence_tensor_transformer_gb300 import synth
+    return synth.BOUNDARY_D4096
+
+
+def flops_per_step(cfg) -> float:
+    return 6.0 * cfg.M * cfg.d * cfg.F
+
+
+def config_json(cfg, extra=None):
+    c = {"workload": cfg.name, "M": cfg.M, "d": cfg.d, "F": cfg.F, "P": cfg.P, "chunks": cfg.chunks,
+         "eps": cfg.eps, "l2": "inputs larger than L2 (no flush): x+partials 192 MB, weights 352 MB per step",
+         "weights": "resident in HBM (model state); activations are the per-step inputs"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        j = json.load(open(path))
+        return {"bf16_burst": j["bf16_tflops"], "bf16_sustained": j["bf16_tflops_sustained"],
+                "hbm": j["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.samples = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append(parts)
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return None
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        pw = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in self.samples for n, v in zip(names, s[4:]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None, "samples": len(self.samples),
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        pg = dist
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local, pg
+
+
+def barrier(pg, device):
+    import torch
+    if pg is not None:
+        if device.type == "cuda":
+            pg.barrier(device_ids=[device.index])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, value: float, device) -> float:
+    import torch
+    if pg is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU baseline (the oracle)
+
+def oracle_rate(cfg, rows: int, inp_f64=None):
+    """Times the float64 oracle on `rows` token rows of the workload on the
+    host cores; returns (seconds, rows)."""
+    import oracle
+    from sequence_tensor_transformer_gb300 import synth
+    if inp_f64 is None:
+        inp_f64 = oracle_inputs(cfg, rows)
+    f = inp_f64
+    t0 = time.perf_counter()
+    oracle.sptp_ffn_forward(f["x"], f["partials"], f["gamma"], f["W1g"], f["W1u"], f["W2"], cfg.P, 1, cfg.eps)
+    return time.perf_counter() - t0
+
+
+def oracle_inputs(cfg, rows: int):
+    from sequence_tensor_transformer_gb300 import synth
+    inp = synth.boundary_inputs(cfg)
+    return {"x": synth.to_f64(inp["x"][:rows], cfg.dtype),
+            "partials": synth.to_f64(inp["partials"][:, :rows], cfg.dtype),
+            "gamma": synth.to_f64(inp["gamma"], cfg.dtype), "W1g": synth.to_f64(inp["W1g"], cfg.dtype),
+            "W1u": synth.to_f64(inp["W1u"], cfg.dtype), "W2": synth.to_f64(inp["W2"], cfg.dtype)}
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, rows=512):
+    f = oracle_inputs(cfg, rows)
+    oracle_rate(cfg, 8, {k: (v[:8] if k == "x" else v[:, :8] if k == "partials" else v) for k, v in f.items()})
+    sec = oracle_rate(cfg, rows, f)
+    tflops = 6.0 * rows * cfg.d * cfg.F / sec / 1e12
+    return {"value": tflops, "unit": UNIT, "tokens_per_s": rows / sec, "cores": cores(), "kind": "oracle",
+            "sample": f"first {rows} of {cfg.M} token rows of the workload (rows are independent), float64 numpy "
+                      f"oracle, {sec:.2f} s"}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cfg = workload()
+    # size each step so that warmup + steps take about a minute
+    probe_rows = 32
+    f = oracle_inputs(cfg, 1024)
+    sub = lambda r: {k: (v[:r] if k == "x" else v[:, :r] if k == "partials" else v) for k, v in f.items()}
+    t = oracle_rate(cfg, probe_rows, sub(probe_rows))
+    per_row = t / probe_rows
+    budget = 60.0
+    rows = int(max(1, min(1024, budget / max(1, args.steps + args.warmup) / per_row)))
+    inp = sub(rows)
+    for _ in range(args.warmup):
+        oracle_rate(cfg, rows, inp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_rate(cfg, rows, inp)
+    sec = time.perf_counter() - t0
+    per_step = sec / args.steps
+    value = 6.0 * rows * cfg.d * cfg.F / per_step / 1e12
+    sample = (f"each step: first {rows} of {cfg.M} token rows of the workload (rows are independent), "
+              f"float64 numpy oracle on the host cores")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "tokens_per_s": rows / per_step,
+            "config": config_json(cfg, {"rows_per_step": rows}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    j = json.load(open(path)).get(kernel)
+    if not j:
+        return None
+    src = os.path.join(ROOT, "sequence_tensor_transformer_gb300", "csrc", j["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != j["source_sha"]:
+        return None
+    return j["bytes_per_launch"]
+
+
+def run_ours(args):
+    import torch
+    import sequence_tensor_transformer_gb300 as st
+    from sequence_tensor_transformer_gb300 import synth
+
+    world, rank, local, pg = dist_setup(args)
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st.load_library()
+    cfg = workload()
+    M, d, F, P, C = cfg.M, cfg.d, cfg.F, cfg.P, cfg.chunks
+    inp = synth.boundary_inputs(cfg)
+
+    def to_dev(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    T = {k: to_dev(v) for k, v in inp.items()}
+    out = torch.empty((P, M, d), dtype=torch.bfloat16, device=dev)
+    resid = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(st.sptp_ffn_workspace_size(M, d, F, P, C, st.SPTP_BF16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P, C, cfg.eps,
+                            out=out, resid_out=resid, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if st.sptp_read_device_status(ws) != 0:
+        raise RuntimeError("device status reports a timeout")
+
+    # ---------------- timed region: K whole-boundary steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg, dev)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(pg, dev)
+    ms_total = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    ms_step = ms_total / args.steps
+    fl = flops_per_step(cfg)
+    value = fl * world / (ms_step * 1e-3) / 1e12
+    tokens = M * world / (ms_step * 1e-3)
+
+    # ---------------- per-kernel durations: the same three kernels launched
+    # through the step-level entry points with events between them
+    y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    s_buf = torch.empty((P, M, F // P), dtype=torch.bfloat16, device=dev)
+    hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
+    n_k = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_k)]
+    for _ in range(3):
+        st.sptp_prologue(T["x"], T["partials"], T["gamma"], cfg.eps, h_out=resid, y_out=y)
+        st.sptp_gateup_swiglu(y, T["W1g"], T["W1u"], P, s_out=s_buf, workspace=hdr)
+        st.sptp_down_proj(s_buf, T["W2"], P, out=out, workspace=hdr)
+    torch.cuda.synchronize()
+    for i in range(n_k):
+        ev[i][0].record(stream)
+        st.sptp_prologue(T["x"], T["partials"], T["gamma"], cfg.eps, h_out=resid, y_out=y)
+        ev[i][1].record(stream)
+        st.sptp_gateup_swiglu(y, T["W1g"], T["W1u"], P, s_out=s_buf, workspace=hdr)
+        ev[i][2].record(stream)
+        st.sptp_down_proj(s_buf, T["W2"], P, out=out, workspace=hdr)
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    ms = {k: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(n_k))
+          for j, k in enumerate(("prologue", "gateup_swiglu", "down_proj"))}
+    pk = peaks()
+    gate_fl = 4.0 * M * d * F
+    down_fl = 2.0 * M * F * d
+    pro_bytes = ((P + 1) * M * d + 2 * M * d) * 2 + 2 * d
+    kernels = {
+        "prologue": {"ms": ms["prologue"], "bound": "hbm", "algorithmic_bytes": pro_bytes,
+                     "achieved": pro_bytes / (ms["prologue"] * 1e-3) / 1e9, "unit": "GB/s",
+                     "peak": pk["hbm"], "traffic": kernel_traffic("prologue")},
+        "gateup_swiglu": {"ms": ms["gateup_swiglu"], "bound": "tensor", "algorithmic_flops": gate_fl,
+                          "achieved": gate_fl / (ms["gateup_swiglu"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "peak": pk["bf16_sustained"], "traffic": kernel_traffic("gateup_swiglu")},
+        "down_proj": {"ms": ms["down_proj"], "bound": "tensor", "algorithmic_flops": down_fl,
+                      "achieved": down_fl / (ms["down_proj"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "peak": pk["bf16_sustained"], "traffic": kernel_traffic("down_proj")},
+    }
+    for k in kernels.values():
+        k["frac"] = k["achieved"] / k["peak"]
+    top = kernels["gateup_swiglu"]
+    roofline = {"bound": "tensor", "kernel": "tc_gemm_kernel<SwiGLU> (gate/up + SwiGLU)",
+                "achieved": top["achieved"], "peak": top["peak"], "unit": "TFLOP/s", "frac": top["frac"],
+                "traffic": top["traffic"],
+                "peak_kind": f"bf16_tflops_sustained ({pk['source']}); burst frac "
+                             f"{top['achieved'] / pk['bf16_burst']:.3f}"}
+
+    # ---------------- end to end through the public call with host buffers
+    pin = {k: torch.empty(T[k].shape, dtype=torch.bfloat16).pin_memory() for k in ("x", "partials")}
+    for k in pin:
+        pin[k].copy_(T[k].cpu())
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    res_h = torch.empty(resid.shape, dtype=torch.bfloat16).pin_memory()
+    xd, pd = torch.empty_like(T["x"]), torch.empty_like(T["partials"])
+
+    def e2e_step():
+        xd.copy_(pin["x"], non_blocking=True)
+        pd.copy_(pin["partials"], non_blocking=True)
+        st.sptp_ffn_forward(xd, pd, T["gamma"], T["W1g"], T["W1u"], T["W2"], P, C, cfg.eps, out=out,
+                            resid_out=resid, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        res_h.copy_(resid, non_blocking=True)
+
+    n_e = max(1, min(args.e2e_steps, args.steps))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(pg, dev)
+    e0.record(stream)
+    for _ in range(n_e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(pg, e0.elapsed_time(e1), dev) / n_e
+    h2d = (pin["x"].numel() + pin["partials"].numel()) * 2
+    d2h = (out_h.numel() + res_h.numel()) * 2
+    e2e = {"value": fl * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
+           "tokens_per_s": M * world / (ms_e2e * 1e-3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": n_e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)-family init)",
+                "tokens_per_s": tokens,
+                "frac_of_bf16_peak": {"sustained": value / world / pk["bf16_sustained"],
+                                      "burst": value / world / pk["bf16_burst"]},
+                "config": config_json(cfg, {"parallelism": f"replicas x{world} (P={P} shards emulated per GPU)"}),
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 3 * args.steps, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,186 @@
+/*
+ * sptp.h -- C ABI of the GB300 (sm_103a) SP-TP FFN boundary library (libsptp.so).
+ *
+ * The library computes the sequence-parallel tensor-parallel (SP-TP) FFN
+ * sub-layer boundary of a Megatron-style transformer with the P tensor-parallel
+ * shards held as P buffers on ONE GPU, and a Delayed-TP stack of FFN sub-layers.
+ *
+ * Sources (web pages, by title and section):
+ *   [A] "[Feature] Async Tensor Parallelism for Archon Engine",
+ *       "TP Communication Is on Activations, Not Weights" and "Potential
+ *       Solution" (chunked all-gather + matmul; the boundary reduce-scatter ->
+ *       residual add + RMSNorm -> all-gather; norm(all_gather(x)) ==
+ *       all_gather(norm(x))).
+ *   [B] "Affinity-Aware Sharding for Delayed Tensor Parallelism", Abstract
+ *       (Delayed TP; contiguous neuron sharding).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     row-major and densely packed unless stated.  The caller owns every
+ *     buffer; the library allocates no memory and keeps no data between calls.
+ *   - Element type is given by `dtype` (sptp_dtype): SPTP_BF16 (compute in
+ *     fp32, store bf16; tcgen05 tensor-core GEMMs) or SPTP_FP32 (fp32
+ *     throughout; CUDA-core GEMMs).  `gamma` and all weights use the same type.
+ *   - Weights use the [out][in] layout: W1g, W1u are [F][d], W2 is [d][F].
+ *     Shard p owns neurons F_p = [p*F/P, (p+1)*F/P): rows F_p of W1g/W1u and
+ *     columns F_p of W2 ([B], contiguous layout).
+ *   - Work is enqueued asynchronously on `cuda_stream` (a cudaStream_t; NULL
+ *     is the legacy default stream).  Nothing is synchronised.
+ *   - Errors are returned as negative sptp_status codes; argument errors are
+ *     detected before any CUDA call, so an error leaves all buffers untouched.
+ *     SPTP_ERR_CUDA reports a launch failure.  A device-side wait that runs
+ *     out (see sptp_read_device_status) is reported through the workspace.
+ *   - Shape rules: M >= 0 (M == 0 is a no-op that returns SPTP_OK; the
+ *     activation pointers may then be NULL), d >= 8,
+ *     d % 8 == 0, d <= 16384; F > 0, F % P == 0, (F/P) % 8 == 0;
+ *     1 <= P <= 8.  (Multiples of 8 keep every row 16-byte aligned.)
+ *   - Pointers must be 16-byte aligned.
+ */
+#ifndef SPTP_H
+#define SPTP_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPTP_BF16 = 0, SPTP_FP32 = 1 } sptp_dtype;
+
+typedef enum {
+    SPTP_OK = 0,
+    SPTP_ERR_NULL = -1,          /* a required pointer is NULL */
+    SPTP_ERR_SHAPE = -2,         /* a size or divisibility rule is violated */
+    SPTP_ERR_DTYPE = -3,         /* dtype is not an sptp_dtype */
+    SPTP_ERR_WORKSPACE = -4,     /* ws_bytes smaller than the *_workspace_size query */
+    SPTP_ERR_CUDA = -5,          /* a CUDA runtime call or kernel launch failed */
+    SPTP_ERR_TIMEOUT = -6,       /* a bounded device-side wait ran out */
+    SPTP_ERR_DEVICE = -7,        /* current device is not compute capability 10.3 */
+    SPTP_ERR_ALIAS = -8          /* an output overlaps an input it must not overlap */
+} sptp_status;
+
+/* Bytes at the start of every workspace holding the device status words. */
+#define SPTP_WS_HEADER_BYTES 4096
+
+/* Workspace bytes needed by sptp_ffn_forward for these sizes (0 on bad args).
+ * Layout: header | y [M][d] normed activations | s [P][M][F/P] SwiGLU output. */
+size_t sptp_ffn_workspace_size(int M, int d, int F, int P, int chunks, int dtype);
+
+/*
+ * sptp_ffn_forward -- one SP-TP FFN sub-layer boundary ([A] "Potential
+ * Solution", sub-layer boundary overlap; intra-layer chunked all-gather +
+ * matmul).  For every token row t:
+ *     r       = sum_{p=0}^{P-1} partials[p][t]      (reduce-scatter arithmetic)
+ *     h       = x[t] + r                            (residual add)
+ *     y       = h * gamma / sqrt(mean_j h_j^2 + eps) (RMSNorm)
+ *   and for every shard p (chunk c of y, rows [c*M/chunks, (c+1)*M/chunks),
+ *   is gathered to all shards; on one GPU the gather is the identity):
+ *     s_p     = silu(y W1g[F_p]^T) * (y W1u[F_p]^T)  (column-parallel, SwiGLU)
+ *     out[p]  = s_p W2[:, F_p]^T                    (row-parallel partial)
+ *
+ *   x         [M][d]    residual stream in
+ *   partials  [P][M][d] the previous sub-layer's row-parallel partials
+ *   gamma     [d]       RMSNorm scale
+ *   W1g, W1u  [F][d]    gate / up projections;  W2 [d][F] down projection
+ *   chunks    number of sequence chunks; M % chunks == 0, chunks % P == 0.
+ *             Chunk c belongs to shard floor(c*P/chunks); the GEMMs consume
+ *             chunks in order.
+ *   out       [P][M][d] the next sub-layer's P partials (not reduced).  Must
+ *             not overlap any input or the workspace.
+ *   resid_out [M][d]    h, the new residual stream; may be NULL (not written)
+ *             and may be exactly x (in place).
+ *   workspace at least sptp_ffn_workspace_size(...) bytes, 256-byte aligned.
+ * Numerics (bf16): sums, norm and SwiGLU in fp32; h, y, s and out are each
+ * rounded once to bf16 (round to nearest even).
+ */
+int sptp_ffn_forward(const void* x, const void* partials, const void* gamma,
+                     const void* W1g, const void* W1u, const void* W2,
+                     int M, int d, int F, int P, int chunks, float eps, int dtype,
+                     void* out, void* resid_out,
+                     void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/* Workspace bytes needed by dtp_ffn_stack_forward (0 on bad args).
+ * Layout: header | y [P][M][d] | s [P][M][F/P] | pending ring [S][P][M][d],
+ * S = min(delta + 1, L). */
+size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta, int dtype);
+
+/*
+ * dtp_ffn_stack_forward -- a Delayed-TP stack of L FFN sub-layers ([B],
+ * Abstract).  Shard p keeps its own residual stream x_p = x_shards[p].
+ * Module l on shard p computes o_p^(l) = FFN_l,p(RMSNorm_l(x_p)) with shard
+ * p's neurons; shard p adds o_p^(l) to x_p at once, and another shard q's
+ * o_q^(l) reaches x_p `delta` modules later (before module l + 1 + delta).
+ * delta == 0 is standard TP.  After module L-1 each shard adds its own last
+ * partial and the partials arriving then; `flush` != 0 also adds every
+ * other-shard partial still pending.
+ *
+ *   x_shards [P][M][d]  in/out residual streams (updated in place)
+ *   gamma    [L][d];  W1g, W1u [L][F][d];  W2 [L][d][F]
+ *   delta >= 0; L >= 1; 1 + (P-1)*min(L, delta+1) <= 64.
+ * Numerics (bf16): each stream update is summed in fp32 (own partial first,
+ * then other shards in ascending shard order, then x_p) and rounded to bf16.
+ */
+int dtp_ffn_stack_forward(void* x_shards, const void* gamma,
+                          const void* W1g, const void* W1u, const void* W2,
+                          int M, int d, int F, int P, int L, int delta, int flush,
+                          float eps, int dtype,
+                          void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/* ---- Step-level entry points (the same kernels the two calls above use). ---- */
+
+/*
+ * sptp_prologue -- steps 1-3 of the boundary ([A] "Potential Solution"):
+ * h = x + sum_p partials[p]; y = RMSNorm(h) * gamma.  h_out may be NULL or x.
+ * y_out [M][d] must not overlap the inputs.
+ */
+int sptp_prologue(const void* x, const void* partials, const void* gamma,
+                  int M, int d, int P, float eps, int dtype,
+                  void* h_out, void* y_out, void* cuda_stream);
+
+/*
+ * sptp_gateup_swiglu -- column-parallel gate/up GEMM with the SwiGLU epilogue
+ * for every shard ([A] "Potential Solution"): s[p] = silu(y W1g[F_p]^T) *
+ * (y W1u[F_p]^T), s_out laid out [P][M][F/P].  workspace: at least
+ * SPTP_WS_HEADER_BYTES (status words).
+ */
+int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u,
+                       int M, int d, int F, int P, int dtype, void* s_out,
+                       void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/*
+ * sptp_down_proj -- row-parallel down GEMM per shard ([A] "Potential
+ * Solution"): out[p] = s[p] W2[:, F_p]^T with s [P][M][F/P], out [P][M][d].
+ * workspace: at least SPTP_WS_HEADER_BYTES.
+ */
+int sptp_down_proj(const void* s, const void* W2, int M, int d, int F, int P, int dtype,
+                   void* out, void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/*
+ * sptp_read_device_status -- synchronises `cuda_stream` and returns the
+ * status the kernels recorded in the workspace header since the last call
+ * that reset it (every entry point above resets it when it starts):
+ * SPTP_OK, or SPTP_ERR_TIMEOUT if a bounded device-side wait ran out (the
+ * kernels then stop early and their outputs are undefined).  No counterpart
+ * on the pages: this is the library's own failure detection.
+ */
+int sptp_read_device_status(const void* workspace, void* cuda_stream);
+
+/*
+ * sptp_wait_selftest -- enqueues a one-CTA kernel that waits on a flag in the
+ * workspace header that nothing sets and on an mbarrier that never completes,
+ * each with the bounded wait the GEMM kernels use and a limit of `limit_ns`
+ * nanoseconds; both waits give up and record SPTP_ERR_TIMEOUT.  If
+ * `preset_flag` != 0 the flag is set first and the flag wait succeeds.  Used to
+ * test failure detection without hanging the GPU.  No counterpart on the pages.
+ */
+int sptp_wait_selftest(void* workspace, size_t ws_bytes, unsigned long long limit_ns,
+                       int preset_flag, void* cuda_stream);
+
+/* Human-readable text of a status code (static storage). */
+const char* sptp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPTP_H */

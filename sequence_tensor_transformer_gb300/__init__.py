@@ -1,0 +1,203 @@
+"""GB300 (sm_103a) SP-TP FFN boundary and Delayed-TP stack.
+
+Thin ctypes binding over libsptp.so: every function here marshals torch
+tensors (device memory) and the current CUDA stream into the C ABI declared
+in include/sptp.h and raises on a non-zero status.  All computation runs in
+the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "SPTP_BF16", "SPTP_FP32", "SPTP_WS_HEADER_BYTES", "SptpError", "lib", "load_library",
+    "sptp_ffn_workspace_size", "sptp_ffn_forward", "dtp_ffn_stack_workspace_size",
+    "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
+    "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "EXPORTED_SYMBOLS",
+]
+
+SPTP_BF16 = 0
+SPTP_FP32 = 1
+SPTP_WS_HEADER_BYTES = 4096
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsptp.so")
+
+EXPORTED_SYMBOLS = (
+    "sptp_ffn_workspace_size", "sptp_ffn_forward", "dtp_ffn_stack_workspace_size",
+    "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
+    "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string",
+)
+
+_lib = None
+
+_P, _I, _F, _Z, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_ulonglong
+_SIGS = {
+    "sptp_ffn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "sptp_ffn_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _Z, _P]),
+    "dtp_ffn_stack_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "dtp_ffn_stack_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P]),
+    "sptp_prologue": (_I, [_P, _P, _P, _I, _I, _I, _F, _I, _P, _P, _P]),
+    "sptp_gateup_swiglu": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "sptp_down_proj": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "sptp_read_device_status": (_I, [_P, _P]),
+    "sptp_wait_selftest": (_I, [_P, _Z, _U64, _I, _P]),
+    "sptp_status_string": (ctypes.c_char_p, [_I]),
+}
+
+
+class SptpError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {code} ({sptp_status_string(code)})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libsptp.so (built by sequence_tensor_transformer_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib_ = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(lib_, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib_
+    return _lib
+
+
+def lib():
+    return load_library()
+
+
+def sptp_status_string(code: int) -> str:
+    return lib().sptp_status_string(int(code)).decode()
+
+
+# ------------------------------------------------------------------ helpers
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPTP_BF16
+    if t.dtype == torch.float32:
+        return SPTP_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensors only")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise SptpError(fn, code)
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, SPTP_WS_HEADER_BYTES), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ entry points
+
+def sptp_ffn_workspace_size(M, d, F, P, chunks, dtype=SPTP_BF16) -> int:
+    return int(lib().sptp_ffn_workspace_size(M, d, F, P, chunks, dtype))
+
+
+def dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dtype=SPTP_BF16) -> int:
+    return int(lib().dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dtype))
+
+
+def sptp_ffn_forward(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, out=None, resid_out=None,
+                     workspace=None, stream=None, write_resid=True):
+    """SP-TP FFN boundary.  Returns (out [P,M,d], resid_out [M,d] or None)."""
+    M, d = x.shape
+    F = W1g.shape[0]
+    dt = _dtype_code(x)
+    if out is None:
+        out = torch.empty((P, M, d), dtype=x.dtype, device=x.device)
+    if resid_out is None and write_resid:
+        resid_out = torch.empty_like(x)
+    if workspace is None:
+        workspace = _workspace(sptp_ffn_workspace_size(M, d, F, P, chunks, dt), x.device)
+    code = lib().sptp_ffn_forward(
+        _ptr(x), _ptr(partials), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, chunks,
+        float(eps), dt, _ptr(out), _ptr(resid_out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("sptp_ffn_forward", code)
+    return out, resid_out
+
+
+def dtp_ffn_stack_forward(x_shards, gamma, W1g, W1u, W2, P, L, delta, flush, eps, workspace=None,
+                          stream=None):
+    """Delayed-TP stack; updates x_shards [P,M,d] in place and returns it."""
+    _, M, d = x_shards.shape
+    F = W1g.shape[1]
+    dt = _dtype_code(x_shards)
+    if workspace is None:
+        workspace = _workspace(dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dt), x_shards.device)
+    code = lib().dtp_ffn_stack_forward(
+        _ptr(x_shards), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, L, delta, int(flush),
+        float(eps), dt, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("dtp_ffn_stack_forward", code)
+    return x_shards
+
+
+def sptp_prologue(x, partials, gamma, eps, h_out=None, y_out=None, stream=None, write_h=True):
+    M, d = x.shape
+    P = partials.shape[0]
+    if y_out is None:
+        y_out = torch.empty_like(x)
+    if h_out is None and write_h:
+        h_out = torch.empty_like(x)
+    code = lib().sptp_prologue(_ptr(x), _ptr(partials), _ptr(gamma), M, d, P, float(eps), _dtype_code(x),
+                               _ptr(h_out), _ptr(y_out), _stream(stream))
+    _check("sptp_prologue", code)
+    return h_out, y_out
+
+
+def sptp_gateup_swiglu(y, W1g, W1u, P, s_out=None, workspace=None, stream=None):
+    M, d = y.shape
+    F = W1g.shape[0]
+    if s_out is None:
+        s_out = torch.empty((P, M, F // P), dtype=y.dtype, device=y.device)
+    if workspace is None:
+        workspace = _workspace(SPTP_WS_HEADER_BYTES, y.device)
+    code = lib().sptp_gateup_swiglu(_ptr(y), _ptr(W1g), _ptr(W1u), M, d, F, P, _dtype_code(y), _ptr(s_out),
+                                    _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("sptp_gateup_swiglu", code)
+    return s_out
+
+
+def sptp_down_proj(s, W2, P, out=None, workspace=None, stream=None):
+    _, M, f = s.shape
+    d, F = W2.shape
+    if out is None:
+        out = torch.empty((P, M, d), dtype=s.dtype, device=s.device)
+    if workspace is None:
+        workspace = _workspace(SPTP_WS_HEADER_BYTES, s.device)
+    code = lib().sptp_down_proj(_ptr(s), _ptr(W2), M, d, F, P, _dtype_code(s), _ptr(out), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    _check("sptp_down_proj", code)
+    return out
+
+
+def sptp_read_device_status(workspace, stream=None) -> int:
+    return int(lib().sptp_read_device_status(_ptr(workspace), _stream(stream)))
+
+
+def sptp_wait_selftest(workspace, limit_ns: int, preset_flag: bool, stream=None) -> int:
+    return int(lib().sptp_wait_selftest(_ptr(workspace), workspace.numel(), int(limit_ns), int(preset_flag),
+                                        _stream(stream)))

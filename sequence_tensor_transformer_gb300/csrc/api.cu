@@ -1,0 +1,491 @@
+// C ABI of libsptp.so: argument validation, workspace layout and the launch
+// sequence of the SP-TP FFN boundary and of the Delayed-TP stack.  Every step
+// of the computation runs in the library's own kernels (prologue.cu,
+// gemm_tc.cu, gemm_simt.cu); this file only checks arguments, lays out the
+// caller's workspace, encodes TMA descriptors and enqueues launches.
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sptp.h"
+#include "sptp_internal.h"
+
+using namespace sptp;
+
+namespace {
+
+constexpr int kMaxD = 16384;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+size_t esize(int dtype) { return dtype == SPTP_BF16 ? 2 : 4; }
+
+bool dtype_ok(int dtype) { return dtype == SPTP_BF16 || dtype == SPTP_FP32; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t an, const void* b, size_t bn) {
+    if (a == nullptr || b == nullptr || an == 0 || bn == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+// Sizes common to both entry points.
+int check_common(int M, int d, int F, int P, int dtype) {
+    if (!dtype_ok(dtype)) return SPTP_ERR_DTYPE;
+    if (M < 0 || d < 8 || d % 8 != 0 || d > kMaxD) return SPTP_ERR_SHAPE;
+    if (P < 1 || P > kMaxGroups) return SPTP_ERR_SHAPE;
+    if (F <= 0 || F % P != 0 || (F / P) % 8 != 0) return SPTP_ERR_SHAPE;
+    if (static_cast<long long>(M) * F >= (1ll << 40)) return SPTP_ERR_SHAPE;
+    return SPTP_OK;
+}
+
+struct DevInfo {
+    int sms = 0;
+    int major = 0, minor = 0;
+};
+
+// Per-device SM count and compute capability, queried once per device.
+int device_info(DevInfo* out) {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPTP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DevInfo di;
+        if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return SPTP_ERR_CUDA;
+        cache[dev] = di;
+        have[dev] = true;
+    }
+    *out = cache[dev];
+    if (out->major != 10 || out->minor != 3) return SPTP_ERR_DEVICE;
+    return SPTP_OK;
+}
+
+DeviceStatus* ws_status(void* ws) { return reinterpret_cast<DeviceStatus*>(ws); }
+
+int reset_status(void* ws, cudaStream_t s) {
+    return cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), s) == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA; }
+
+const char* cptr(const void* base, size_t off_bytes) { return static_cast<const char*>(base) + off_bytes; }
+char* mptr(void* base, size_t off_bytes) { return static_cast<char*>(base) + off_bytes; }
+
+// ------------------------------------------------------------- GEMM launches
+
+constexpr int kBM = 128, kBNSwiGLU = 128, kBNStore = 256, kBK = 64;
+
+// Gate/up + SwiGLU for P groups: s_g = silu(A_g W1g[F_g]^T) * (A_g W1u[F_g]^T).
+int gateup(const void* const* A, const void* W1g, const void* W1u, int M, int d, int F, int P, int dtype,
+           void* s_out, DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
+    const int f = F / P;
+    const size_t es = esize(dtype);
+    if (M == 0) return SPTP_OK;
+    if (dtype == SPTP_BF16) {
+        TcGemmParams p;
+        std::memset(&p, 0, sizeof(p));
+        for (int g = 0; g < P; ++g) {
+            const size_t woff = static_cast<size_t>(g) * f * d * es;
+            if (!encode_map_bf16(&p.mapA[g], A[g], d, M, static_cast<uint64_t>(d) * es, kBK, kBM) ||
+                !encode_map_bf16(&p.mapB0[g], cptr(W1g, woff), d, f, static_cast<uint64_t>(d) * es, kBK,
+                                 kBNSwiGLU) ||
+                !encode_map_bf16(&p.mapB1[g], cptr(W1u, woff), d, f, static_cast<uint64_t>(d) * es, kBK,
+                                 kBNSwiGLU))
+                return SPTP_ERR_CUDA;
+            p.out[g] = mptr(s_out, static_cast<size_t>(g) * M * f * es);
+        }
+        p.ldo = f;
+        p.M = M;
+        p.N = f;
+        p.K = d;
+        p.G = P;
+        p.mt = (M + kBM - 1) / kBM;
+        p.nt = (f + kBNSwiGLU - 1) / kBNSwiGLU;
+        p.nk = (d + kBK - 1) / kBK;
+        p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
+        p.status = st;
+        p.wait_limit_ns = kWaitLimitNs;
+        return cuda_status(launch_tc_gemm(p, Epi::kSwiGLU, di.sms, s));
+    }
+    SimtGemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int g = 0; g < P; ++g) {
+        const size_t woff = static_cast<size_t>(g) * f * d;
+        p.A[g] = static_cast<const float*>(A[g]);
+        p.B0[g] = static_cast<const float*>(W1g) + woff;
+        p.B1[g] = static_cast<const float*>(W1u) + woff;
+        p.C[g] = static_cast<float*>(s_out) + static_cast<size_t>(g) * M * f;
+    }
+    p.lda = d;
+    p.ldb = d;
+    p.ldc = f;
+    p.M = M;
+    p.N = f;
+    p.K = d;
+    p.G = P;
+    return cuda_status(launch_simt_gemm(p, Epi::kSwiGLU, s));
+}
+
+// Down projection for P groups: out_g = s_g W2[:, F_g]^T.
+int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype, void* const* out,
+         DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
+    const int f = F / P;
+    const size_t es = esize(dtype);
+    if (M == 0) return SPTP_OK;
+    if (dtype == SPTP_BF16) {
+        TcGemmParams p;
+        std::memset(&p, 0, sizeof(p));
+        for (int g = 0; g < P; ++g) {
+            if (!encode_map_bf16(&p.mapA[g], cptr(s_in, static_cast<size_t>(g) * M * f * es), f, M,
+                                 static_cast<uint64_t>(f) * es, kBK, kBM) ||
+                !encode_map_bf16(&p.mapB0[g], cptr(W2, static_cast<size_t>(g) * f * es), f, d,
+                                 static_cast<uint64_t>(F) * es, kBK, kBNStore))
+                return SPTP_ERR_CUDA;
+            p.out[g] = out[g];
+        }
+        p.ldo = d;
+        p.M = M;
+        p.N = d;
+        p.K = f;
+        p.G = P;
+        p.mt = (M + kBM - 1) / kBM;
+        p.nt = (d + kBNStore - 1) / kBNStore;
+        p.nk = (f + kBK - 1) / kBK;
+        p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
+        p.status = st;
+        p.wait_limit_ns = kWaitLimitNs;
+        return cuda_status(launch_tc_gemm(p, Epi::kStore, di.sms, s));
+    }
+    SimtGemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int g = 0; g < P; ++g) {
+        p.A[g] = static_cast<const float*>(s_in) + static_cast<size_t>(g) * M * f;
+        p.B0[g] = static_cast<const float*>(W2) + static_cast<size_t>(g) * f;
+        p.B1[g] = nullptr;
+        p.C[g] = static_cast<float*>(out[g]);
+    }
+    p.lda = f;
+    p.ldb = F;
+    p.ldc = d;
+    p.M = M;
+    p.N = d;
+    p.K = f;
+    p.G = P;
+    return cuda_status(launch_simt_gemm(p, Epi::kStore, s));
+}
+
+// Raster band (m-tiles walked together) from the sequence chunk height.
+int band_for_chunks(int M, int chunks) {
+    const int rows = chunks > 0 ? M / chunks : M;
+    int band = rows / kBM;
+    if (band < 1 || rows % kBM != 0) band = 8;
+    if (band > 16) band = 16;
+    return band;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sptp_status_string(int status) {
+    switch (status) {
+        case SPTP_OK: return "ok";
+        case SPTP_ERR_NULL: return "a required pointer is NULL";
+        case SPTP_ERR_SHAPE: return "a size or divisibility rule is violated";
+        case SPTP_ERR_DTYPE: return "unknown dtype";
+        case SPTP_ERR_WORKSPACE: return "workspace too small";
+        case SPTP_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+        case SPTP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+        case SPTP_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
+        case SPTP_ERR_ALIAS: return "an output overlaps an input";
+        default: return "unknown status";
+    }
+}
+
+size_t sptp_ffn_workspace_size(int M, int d, int F, int P, int chunks, int dtype) {
+    if (check_common(M, d, F, P, dtype) != SPTP_OK || chunks < 1) return 0;
+    const size_t es = esize(dtype);
+    return SPTP_WS_HEADER_BYTES + align_up(static_cast<size_t>(M) * d * es) +
+           align_up(static_cast<size_t>(M) * F * es);
+}
+
+int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, const void* W1g, const void* W1u,
+                     const void* W2, int M, int d, int F, int P, int chunks, float eps, int dtype, void* out,
+                     void* resid_out, void* workspace, size_t ws_bytes, void* cuda_stream) {
+    // activations of an empty sequence (M == 0) may be NULL
+    if (!gamma || !W1g || !W1u || !W2 || !workspace || (M != 0 && (!x || !partials || !out)))
+        return SPTP_ERR_NULL;
+    int rc = check_common(M, d, F, P, dtype);
+    if (rc != SPTP_OK) return rc;
+    if (chunks < 1 || chunks % P != 0 || (M > 0 && M % chunks != 0)) return SPTP_ERR_SHAPE;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
+    const void* ptrs[] = {x, partials, gamma, W1g, W1u, W2, out, resid_out, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return SPTP_ERR_SHAPE;
+    const size_t need = sptp_ffn_workspace_size(M, d, F, P, chunks, dtype);
+    if (ws_bytes < need) return SPTP_ERR_WORKSPACE;
+    const size_t es = esize(dtype);
+    const size_t act = static_cast<size_t>(M) * d * es;
+    const size_t out_bytes = act * P;
+    const size_t wg = static_cast<size_t>(F) * d * es;
+    // out must not overlap anything it is computed from or the workspace
+    const void* ins[] = {x, partials, gamma, W1g, W1u, W2, workspace, resid_out};
+    const size_t insz[] = {act, out_bytes, d * es, wg, wg, wg, need, resid_out ? act : 0};
+    for (int i = 0; i < 8; ++i)
+        if (overlaps(out, out_bytes, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    const void* wins[] = {x, partials, gamma, W1g, W1u, W2};
+    const size_t wsz[] = {act, out_bytes, d * es, wg, wg, wg};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(workspace, need, wins[i], wsz[i])) return SPTP_ERR_ALIAS;
+    if (resid_out && resid_out != x) {
+        const void* rins[] = {x, partials, gamma, W1g, W1u, W2, workspace};
+        const size_t rsz[] = {act, out_bytes, d * es, wg, wg, wg, need};
+        for (int i = 0; i < 7; ++i)
+            if (overlaps(resid_out, act, rins[i], rsz[i])) return SPTP_ERR_ALIAS;
+    }
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+
+    void* y = mptr(workspace, SPTP_WS_HEADER_BYTES);
+    void* sbuf = mptr(workspace, SPTP_WS_HEADER_BYTES + align_up(act));
+
+    // 1-3: reduce-scatter arithmetic, residual add, RMSNorm (every chunk)
+    PrologueParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.G = 1;
+    pp.M = M;
+    pp.d = d;
+    pp.eps = eps;
+    pp.gamma = gamma;
+    pp.grp[0] = PrologueGroup{x, resid_out, y, 0, P};
+    for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
+    if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
+
+    // 4-6: chunked gather (identity) + column-parallel gate/up + SwiGLU,
+    // tiles walked chunk by chunk
+    const void* A[kMaxGroups];
+    for (int g = 0; g < P; ++g) A[g] = y;
+    const int band = band_for_chunks(M, chunks);
+    if ((rc = gateup(A, W1g, W1u, M, d, F, P, dtype, sbuf, ws_status(workspace), band, di, s)) != SPTP_OK)
+        return rc;
+
+    // 7: row-parallel down projection, one partial per shard
+    void* outs[kMaxGroups];
+    for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * act);
+    return down(sbuf, W2, M, d, F, P, dtype, outs, ws_status(workspace), band, di, s);
+}
+
+size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta, int dtype) {
+    if (check_common(M, d, F, P, dtype) != SPTP_OK || L < 1 || delta < 0) return 0;
+    const size_t es = esize(dtype);
+    const size_t S = static_cast<size_t>(delta + 1 < L ? delta + 1 : L);
+    const size_t act = static_cast<size_t>(M) * d * es;
+    return SPTP_WS_HEADER_BYTES + align_up(act * P) + align_up(static_cast<size_t>(M) * F * es) +
+           align_up(S * P * act);
+}
+
+int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, const void* W1u, const void* W2,
+                          int M, int d, int F, int P, int L, int delta, int flush, float eps, int dtype,
+                          void* workspace, size_t ws_bytes, void* cuda_stream) {
+    if (!gamma || !W1g || !W1u || !W2 || !workspace || (M != 0 && !x_shards)) return SPTP_ERR_NULL;
+    int rc = check_common(M, d, F, P, dtype);
+    if (rc != SPTP_OK) return rc;
+    if (L < 1 || delta < 0) return SPTP_ERR_SHAPE;
+    const int S = delta + 1 < L ? delta + 1 : L;
+    if (1 + (P - 1) * S > kMaxSrcPerGroup) return SPTP_ERR_SHAPE;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
+    const void* ptrs[] = {x_shards, gamma, W1g, W1u, W2, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return SPTP_ERR_SHAPE;
+    const size_t need = dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dtype);
+    if (ws_bytes < need) return SPTP_ERR_WORKSPACE;
+    const size_t es = esize(dtype);
+    const size_t act = static_cast<size_t>(M) * d * es;
+    const size_t wg = static_cast<size_t>(L) * F * d * es;
+    const void* ins[] = {gamma, W1g, W1u, W2, workspace};
+    const size_t insz[] = {static_cast<size_t>(L) * d * es, wg, wg, wg, need};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(x_shards, act * P, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+
+    const int f = F / P;
+    char* ybase = mptr(workspace, SPTP_WS_HEADER_BYTES);
+    char* sbuf = ybase + align_up(act * P);
+    char* ring = sbuf + align_up(static_cast<size_t>(M) * F * es);
+    auto xs = [&](int p) { return mptr(x_shards, static_cast<size_t>(p) * act); };
+    auto yp = [&](int p) { return ybase + static_cast<size_t>(p) * act; };
+    auto o = [&](int l, int p) { return ring + (static_cast<size_t>(l % S) * P + p) * act; };
+
+    const void* A[kMaxGroups];
+    void* outs[kMaxGroups];
+    for (int l = 0; l <= L; ++l) {
+        // stream update before module l (or the final one at l == L):
+        // own partial of module l-1, other shards' partials of module l-1-delta
+        // and, at the end with flush, every other-shard partial still pending
+        PrologueParams pp;
+        std::memset(&pp, 0, sizeof(pp));
+        pp.G = P;
+        pp.M = M;
+        pp.d = d;
+        pp.eps = eps;
+        pp.gamma = l < L ? cptr(gamma, static_cast<size_t>(l) * d * es) : gamma;
+        int ns = 0;
+        for (int p = 0; p < P; ++p) {
+            const int begin = ns;
+            if (l >= 1) pp.src[ns++] = o(l - 1, p);
+            const int k = l - 1 - delta;
+            if (k >= 0)
+                for (int q = 0; q < P; ++q)
+                    if (q != p) pp.src[ns++] = o(k, q);
+            if (l == L && flush)
+                for (int kk = (L - delta > 0 ? L - delta : 0); kk < L; ++kk)
+                    for (int q = 0; q < P; ++q)
+                        if (q != p) pp.src[ns++] = o(kk, q);
+            pp.grp[p] = PrologueGroup{xs(p), xs(p), l < L ? yp(p) : nullptr, begin, ns - begin};
+        }
+        if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
+        if (l == L) break;
+
+        const size_t woff = static_cast<size_t>(l) * F * d * es;
+        for (int p = 0; p < P; ++p) A[p] = yp(p);
+        if ((rc = gateup(A, cptr(W1g, woff), cptr(W1u, woff), M, d, F, P, dtype, sbuf, ws_status(workspace), 8,
+                         di, s)) != SPTP_OK)
+            return rc;
+        for (int p = 0; p < P; ++p) outs[p] = o(l, p);
+        if ((rc = down(sbuf, cptr(W2, woff), M, d, F, P, dtype, outs, ws_status(workspace), 8, di, s)) !=
+            SPTP_OK)
+            return rc;
+        (void)f;
+    }
+    return SPTP_OK;
+}
+
+int sptp_prologue(const void* x, const void* partials, const void* gamma, int M, int d, int P, float eps,
+                  int dtype, void* h_out, void* y_out, void* cuda_stream) {
+    if (!gamma || (M != 0 && (!x || !partials || !y_out))) return SPTP_ERR_NULL;
+    int rc = check_common(M, d, 8 * P, P, dtype);
+    if (rc != SPTP_OK) return rc;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
+    const void* ptrs[] = {x, partials, gamma, h_out, y_out};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    const size_t es = esize(dtype);
+    const size_t act = static_cast<size_t>(M) * d * es;
+    const void* ins[] = {x, partials, gamma, h_out};
+    const size_t insz[] = {act, act * P, d * es, h_out ? act : 0};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(y_out, act, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    if (h_out && h_out != x && (overlaps(h_out, act, partials, act * P) || overlaps(h_out, act, x, act)))
+        return SPTP_ERR_ALIAS;
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    PrologueParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.G = 1;
+    pp.M = M;
+    pp.d = d;
+    pp.eps = eps;
+    pp.gamma = gamma;
+    pp.grp[0] = PrologueGroup{x, h_out, y_out, 0, P};
+    for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
+    return cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u, int M, int d, int F, int P, int dtype,
+                       void* s_out, void* workspace, size_t ws_bytes, void* cuda_stream) {
+    if (!W1g || !W1u || !workspace || (M != 0 && (!y || !s_out))) return SPTP_ERR_NULL;
+    int rc = check_common(M, d, F, P, dtype);
+    if (rc != SPTP_OK) return rc;
+    const void* ptrs[] = {y, W1g, W1u, s_out, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    if (ws_bytes < SPTP_WS_HEADER_BYTES) return SPTP_ERR_WORKSPACE;
+    const size_t es = esize(dtype);
+    const size_t sb = static_cast<size_t>(M) * F * es, wg = static_cast<size_t>(F) * d * es;
+    if (overlaps(s_out, sb, y, static_cast<size_t>(M) * d * es) || overlaps(s_out, sb, W1g, wg) ||
+        overlaps(s_out, sb, W1u, wg) || overlaps(s_out, sb, workspace, SPTP_WS_HEADER_BYTES))
+        return SPTP_ERR_ALIAS;
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    const void* A[kMaxGroups];
+    for (int g = 0; g < P; ++g) A[g] = y;
+    return gateup(A, W1g, W1u, M, d, F, P, dtype, s_out, ws_status(workspace), 8, di, s);
+}
+
+int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype, void* out,
+                   void* workspace, size_t ws_bytes, void* cuda_stream) {
+    if (!W2 || !workspace || (M != 0 && (!s_in || !out))) return SPTP_ERR_NULL;
+    int rc = check_common(M, d, F, P, dtype);
+    if (rc != SPTP_OK) return rc;
+    const void* ptrs[] = {s_in, W2, out, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    if (ws_bytes < SPTP_WS_HEADER_BYTES) return SPTP_ERR_WORKSPACE;
+    const size_t es = esize(dtype);
+    const size_t ob = static_cast<size_t>(P) * M * d * es;
+    if (overlaps(out, ob, s_in, static_cast<size_t>(M) * F * es) ||
+        overlaps(out, ob, W2, static_cast<size_t>(F) * d * es) ||
+        overlaps(out, ob, workspace, SPTP_WS_HEADER_BYTES))
+        return SPTP_ERR_ALIAS;
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    void* outs[kMaxGroups];
+    for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * M * d * es);
+    return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), 8, di, s);
+}
+
+int sptp_read_device_status(const void* workspace, void* cuda_stream) {
+    if (!workspace) return SPTP_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SPTP_ERR_CUDA;
+    DeviceStatus st;
+    if (cudaMemcpy(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return SPTP_ERR_CUDA;
+    return st.code;
+}
+
+int sptp_wait_selftest(void* workspace, size_t ws_bytes, unsigned long long limit_ns, int preset_flag,
+                       void* cuda_stream) {
+    if (!workspace) return SPTP_ERR_NULL;
+    if (ws_bytes < SPTP_WS_HEADER_BYTES) return SPTP_ERR_WORKSPACE;
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return SPTP_ERR_SHAPE;
+    DevInfo di;
+    int rc = device_info(&di);
+    if (rc != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    if (preset_flag) {
+        static const int one = 1;
+        if (cudaMemcpyAsync(&ws_status(workspace)->flag, &one, sizeof(int), cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+            return SPTP_ERR_CUDA;
+    }
+    return cuda_status(launch_wait_selftest(ws_status(workspace), limit_ns, s));
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// Internal declarations shared by the library's translation units:
+// kernel parameter blocks and host-side launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sptp {
+
+constexpr int kMaxGroups = 8;          // shards per launch (P <= 8)
+constexpr int kMaxSrcPerGroup = 64;    // partial sources summed into one stream
+constexpr int kMaxSrc = kMaxGroups * kMaxSrcPerGroup;
+
+// Device status words at the start of every workspace.
+struct DeviceStatus {
+    int code;       // 0 or SPTP_ERR_TIMEOUT
+    int where;      // which wait gave up (kWhere*)
+    int block;      // blockIdx.x of the first CTA that gave up
+    int info;       // role-specific detail (tile index)
+    int flag;       // test flag for the wait self-test
+};
+
+enum : int {
+    kWhereProducerEmpty = 1,
+    kWhereMmaFull = 2,
+    kWhereMmaAccEmpty = 3,
+    kWhereEpilogueAccFull = 4,
+    kWhereDrain = 5,
+    kWhereSelftestFlag = 6,
+    kWhereSelftestBarrier = 7,
+};
+
+// Default limit of every bounded device-side wait (ns). A legitimate wait in
+// these kernels lasts microseconds.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// ---------------------------------------------------------------- prologue
+struct PrologueGroup {
+    const void* x;   // [M][d]
+    void* h;         // [M][d] or nullptr
+    void* y;         // [M][d] or nullptr (accumulate only, no norm)
+    int src_begin;   // first index into PrologueParams::src
+    int n_src;       // number of partial sources summed into this group
+};
+
+struct PrologueParams {
+    PrologueGroup grp[kMaxGroups];
+    const void* src[kMaxSrc];
+    const void* gamma;   // [d]
+    int G, M, d;
+    float eps;
+};
+
+// Launches the partial-sum + residual + RMSNorm kernel over G groups of M rows.
+cudaError_t launch_prologue(const PrologueParams& p, bool bf16, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- tcgen05 GEMM
+// out_g[m][n] = epilogue( sum_k A_g[m][k] * B_g[n][k] ) for every group g.
+// SwiGLU mode: B_g is the gate block (mapB0) stacked on the up block (mapB1),
+// 128 rows each, and out = silu(gate) * up; plain mode: B_g has 256 rows per
+// tile (mapB0) and out = the bf16-rounded accumulator.
+struct TcGemmParams {
+    CUtensorMap mapA[kMaxGroups];
+    CUtensorMap mapB0[kMaxGroups];
+    CUtensorMap mapB1[kMaxGroups];
+    void* out[kMaxGroups];
+    long long ldo;         // output row stride (elements)
+    int M, N, K;           // rows, output columns, reduction length (per group)
+    int G, mt, nt, nk;     // groups, m-tiles, n-tiles, k-blocks
+    int band;              // m-tiles per raster band
+    DeviceStatus* status;
+    unsigned long long wait_limit_ns;
+};
+
+enum class Epi { kSwiGLU, kStore };
+
+cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
+size_t tc_gemm_smem_bytes();
+
+// Encodes a 2-D bf16 tensor map (inner = contiguous dim) with 128-byte swizzle.
+bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---------------------------------------------------------------- fp32 SIMT GEMM
+struct SimtGemmParams {
+    const float* A[kMaxGroups];
+    const float* B0[kMaxGroups];
+    const float* B1[kMaxGroups];
+    float* C[kMaxGroups];
+    long long lda, ldb, ldc;
+    int M, N, K, G;
+};
+
+cudaError_t launch_simt_gemm(const SimtGemmParams& p, Epi epi, cudaStream_t s);
+
+// ---------------------------------------------------------------- self-test
+cudaError_t launch_wait_selftest(DeviceStatus* st, unsigned long long limit_ns, cudaStream_t s);
+
+}  // namespace sptp

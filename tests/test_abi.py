@@ -1,0 +1,102 @@
+"""CPU tests of the C ABI: the library loads, exports every declared entry
+point, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sequence_tensor_transformer_gb300 as st
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(st.LIB_PATH):
+        from sequence_tensor_transformer_gb300 import build
+        build.build()
+    return st.load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    raw = ctypes.CDLL(st.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(names) == set(st.EXPORTED_SYMBOLS)
+
+
+def test_status_strings(lib):
+    assert st.sptp_status_string(0) == "ok"
+    for c in range(-1, -9, -1):
+        assert st.sptp_status_string(c) != "unknown status"
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address that is never dereferenced
+
+
+def fwd(lib, M=64, d=128, F=512, P=2, C=4, eps=1e-6, dt=0, ptrs=None, out=FAKE * 64, resid=None,
+        ws=FAKE * 4096, ws_bytes=1 << 40):
+    p = ptrs or [FAKE * (i + 1) for i in range(6)]
+    return lib.sptp_ffn_forward(*p, M, d, F, P, C, eps, dt, out, resid, ws, ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments_without_gpu(lib):
+    SHAPE, NULL, DTYPE, WS, ALIAS = -2, -1, -3, -4, -8
+    assert fwd(lib, ptrs=[None] + [FAKE] * 5) == NULL
+    assert fwd(lib, out=None) == NULL
+    assert fwd(lib, ws=None) == NULL
+    assert fwd(lib, d=100) == SHAPE           # d % 8
+    assert fwd(lib, F=500) == SHAPE           # F % P ... (F/P) % 8
+    assert fwd(lib, F=24, P=2) == SHAPE       # F/P = 12 not a multiple of 8
+    assert fwd(lib, P=9, F=9 * 64, C=9) == SHAPE
+    assert fwd(lib, C=3) == SHAPE             # chunks % P
+    assert fwd(lib, M=66, C=4) == SHAPE       # M % chunks
+    assert fwd(lib, dt=7) == DTYPE
+    assert fwd(lib, eps=float("nan")) == SHAPE
+    assert fwd(lib, ws_bytes=10) == WS
+    assert fwd(lib, ptrs=[FAKE + 8] + [FAKE * 2] * 5) == SHAPE   # misaligned
+    # out overlapping an input
+    assert fwd(lib, ptrs=[FAKE * 64] + [FAKE * (i + 2) * 1024 for i in range(5)], out=FAKE * 64) == ALIAS
+
+
+def test_workspace_size_queries(lib):
+    n = st.sptp_ffn_workspace_size(64, 128, 512, 2, 4, 1)
+    assert n >= 4096 + 64 * 128 * 4 + 64 * 512 * 4
+    assert st.sptp_ffn_workspace_size(64, 100, 512, 2, 4, 0) == 0
+    m = st.dtp_ffn_stack_workspace_size(4096, 1024, 3072, 2, 4, 1, 0)
+    act = 4096 * 1024 * 2
+    assert m >= 4096 + 2 * act + 4096 * 3072 * 2 + 2 * 2 * act
+    assert st.dtp_ffn_stack_workspace_size(4096, 1024, 3072, 2, 0, 1, 0) == 0
+
+
+def test_dtp_rejects_bad_arguments_without_gpu(lib):
+    p = [FAKE * (i + 1) * 4096 for i in range(5)]
+    call = lambda **k: lib.dtp_ffn_stack_forward(
+        *p, k.get("M", 64), k.get("d", 128), k.get("F", 512), k.get("P", 2), k.get("L", 2),
+        k.get("delta", 1), 1, 1e-6, 0, FAKE * 64 * 4096, 1 << 40, None)
+    assert call(delta=-1) == -2
+    assert call(L=0) == -2
+    assert call(P=8, F=8 * 64, L=40, delta=40) == -2   # too many pending sources
+    assert lib.dtp_ffn_stack_forward(None, *p[1:], 64, 128, 512, 2, 2, 1, 1, 1e-6, 0, FAKE, 1 << 40, None) == -1
+
+
+def test_step_entry_points_reject_bad_arguments(lib):
+    assert lib.sptp_prologue(FAKE, FAKE * 2, FAKE * 3, 64, 100, 2, 1e-6, 0, None, FAKE * 4, None) == -2
+    assert lib.sptp_prologue(FAKE, FAKE * 2, FAKE * 3, 64, 128, 2, 1e-6, 0, None, None, None) == -1
+    assert lib.sptp_gateup_swiglu(FAKE, FAKE * 2, FAKE * 3, 64, 128, 500, 2, 0, FAKE * 4, FAKE * 5, 1 << 20,
+                                  None) == -2
+    assert lib.sptp_down_proj(FAKE, FAKE * 2, 64, 128, 512, 2, 0, FAKE * 3, FAKE * 4, 100, None) == -4
+    assert lib.sptp_wait_selftest(FAKE, 100, 1000, 0, None) == -4
