@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -85,6 +86,14 @@ char* mptr(void* base, size_t off_bytes) { return static_cast<char*>(base) + off
 
 constexpr int kBM = 128, kBNSwiGLU = 128, kBNStore = 256, kBK = 64;
 
+// The bf16 GEMMs run on CTA pairs (cta_group::2, 256-row tiles) unless the
+// environment variable SPTP_GEMM_VARIANT is "single" (one CTA per tile,
+// 128-row tiles; kept for comparison).
+bool use_pair_gemm() {
+    const char* v = std::getenv("SPTP_GEMM_VARIANT");
+    return !(v != nullptr && std::strcmp(v, "single") == 0);
+}
+
 // Gate/up + SwiGLU for P groups: s_g = silu(A_g W1g[F_g]^T) * (A_g W1u[F_g]^T).
 int gateup(const void* const* A, const void* W1g, const void* W1u, int M, int d, int F, int P, int dtype,
            void* s_out, DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
@@ -104,18 +113,22 @@ int gateup(const void* const* A, const void* W1g, const void* W1u, int M, int d,
                 return SPTP_ERR_CUDA;
             p.out[g] = mptr(s_out, static_cast<size_t>(g) * M * f * es);
         }
+        const bool pair = use_pair_gemm();
+        const int bm = pair ? 2 * kBM : kBM;
         p.ldo = f;
         p.M = M;
         p.N = f;
         p.K = d;
         p.G = P;
-        p.mt = (M + kBM - 1) / kBM;
+        p.mt = (M + bm - 1) / bm;
         p.nt = (f + kBNSwiGLU - 1) / kBNSwiGLU;
         p.nk = (d + kBK - 1) / kBK;
+        if (pair) band = (band + 1) / 2;
         p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
         p.status = st;
         p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(launch_tc_gemm(p, Epi::kSwiGLU, di.sms, s));
+        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kSwiGLU, di.sms, s)
+                                : launch_tc_gemm(p, Epi::kSwiGLU, di.sms, s));
     }
     SimtGemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -143,13 +156,17 @@ int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype
     const size_t es = esize(dtype);
     if (M == 0) return SPTP_OK;
     if (dtype == SPTP_BF16) {
+        const bool pair = use_pair_gemm();
+        const int bm = pair ? 2 * kBM : kBM;
+        // a CTA pair stages each B tile as two 128-row halves
+        const uint32_t bbox = pair ? kBNStore / 2 : kBNStore;
         TcGemmParams p;
         std::memset(&p, 0, sizeof(p));
         for (int g = 0; g < P; ++g) {
             if (!encode_map_bf16(&p.mapA[g], cptr(s_in, static_cast<size_t>(g) * M * f * es), f, M,
                                  static_cast<uint64_t>(f) * es, kBK, kBM) ||
                 !encode_map_bf16(&p.mapB0[g], cptr(W2, static_cast<size_t>(g) * f * es), f, d,
-                                 static_cast<uint64_t>(F) * es, kBK, kBNStore))
+                                 static_cast<uint64_t>(F) * es, kBK, bbox))
                 return SPTP_ERR_CUDA;
             p.out[g] = out[g];
         }
@@ -158,13 +175,15 @@ int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype
         p.N = d;
         p.K = f;
         p.G = P;
-        p.mt = (M + kBM - 1) / kBM;
+        p.mt = (M + bm - 1) / bm;
         p.nt = (d + kBNStore - 1) / kBNStore;
         p.nk = (f + kBK - 1) / kBK;
+        if (pair) band = (band + 1) / 2;
         p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
         p.status = st;
         p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(launch_tc_gemm(p, Epi::kStore, di.sms, s));
+        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kStore, di.sms, s)
+                                : launch_tc_gemm(p, Epi::kStore, di.sms, s));
     }
     SimtGemmParams p;
     std::memset(&p, 0, sizeof(p));

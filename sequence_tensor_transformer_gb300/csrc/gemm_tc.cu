@@ -261,6 +261,247 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant (cta_group::2, cluster of 2): the pair computes a
+// 256 x 256 tile.  Each CTA stages its own 128 A rows and one half of the B
+// tile (SwiGLU: CTA 0 the 128 gate rows, CTA 1 the 128 up rows; plain: the
+// two 128-row halves), so a stage is 32 KiB per CTA and 6 stages fit.  The
+// even CTA issues the UMMAs (M=256, N=256, K=16); both CTAs' TMA loads
+// complete on the even CTA's full barrier; commits are multicast to both
+// CTAs' empty / accumulator-full barriers; both CTAs' epilogues release the
+// accumulator on the even CTA's accumulator-empty barrier.
+namespace pair {
+
+constexpr int PBM = 256;                     // tile rows (128 per CTA)
+constexpr int PBN = 256;                     // UMMA N
+constexpr int PSTAGES = 6;
+constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
+constexpr int B_BYTES = 128 * BK * 2;        // 16 KiB (half of the B tile)
+constexpr int PSTAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + BAR_BYTES;
+constexpr uint32_t PIDESC = idesc_bf16_f32(PBM, PBN);
+
+struct Bars {
+    uint64_t full[PSTAGES];
+    uint64_t empty[PSTAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block too large");
+
+template <Epi EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* a_tiles = smem;
+    uint8_t* b_tiles = smem + PSTAGES * A_BYTES;
+    Bars* bars = reinterpret_cast<Bars*>(smem + PSTAGES * PSTAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars->acc_full[a], 1);
+            mbar_init(&bars->acc_empty[a], 2 * 4 * 32);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int g = 0; g < p.G; ++g) {
+            tma_prefetch_map(&p.mapA[g]);
+            tma_prefetch_map(&p.mapB0[g]);
+            if (EPI == Epi::kSwiGLU) tma_prefetch_map(&p.mapB1[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // peer barriers initialised and peer TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    WaitCtx wc{p.status, &bars->abort_flag, p.wait_limit_ns};
+    const int total = p.G * p.mt * p.nt;
+    const int pair_id = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        const uint32_t full0 = mapa_shared(smem_u32(&bars->full[0]), 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        int armed_parity[PSTAGES];
+        for (int s = 0; s < PSTAGES; ++s) armed_parity[s] = -1;
+        bool ok = true;
+        for (int t = pair_id; ok && t < total; t += npairs) {
+            int g, m, n;
+            decode_tile(p, t, g, m, n);
+            for (int kb = 0; kb < p.nk; ++kb) {
+                if (!mbar_wait(&bars->empty[stage], phase ^ 1u, wc, kWhereProducerEmpty, t)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    mbar_arrive_expect_tx(&bars->full[stage], 2 * PSTAGE_BYTES);
+                    armed_parity[stage] = static_cast<int>(phase);
+                }
+                const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+                tma_load_2d_pair(a_tiles + stage * A_BYTES, &p.mapA[g], fb, kb * BK,
+                                 m * PBM + static_cast<int>(rank) * 128);
+                uint8_t* bt = b_tiles + stage * B_BYTES;
+                if (EPI == Epi::kSwiGLU) {
+                    tma_load_2d_pair(bt, rank == 0 ? &p.mapB0[g] : &p.mapB1[g], fb, kb * BK, n * 128);
+                } else {
+                    tma_load_2d_pair(bt, &p.mapB0[g], fb, kb * BK, n * PBN + static_cast<int>(rank) * 128);
+                }
+                if (++stage == PSTAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        WaitCtx drain{p.status, &bars->abort_flag, p.wait_limit_ns};
+        int dummy_abort = 0;
+        drain.abort_flag = &dummy_abort;
+        if (leader) {
+            // both CTAs' copies complete on the leader's full barriers
+            for (int s = 0; s < PSTAGES; ++s)
+                if (armed_parity[s] >= 0)
+                    mbar_wait(&bars->full[s], static_cast<uint32_t>(armed_parity[s]), drain, kWhereDrain, s);
+        } else if (!ok) {
+            // give copies this CTA may still have in flight time to land
+            const unsigned long long t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int local = 0;
+        for (int t = pair_id; ok && t < total; t += npairs, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, wc, kWhereMmaAccEmpty, t)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PBN);
+            for (int kb = 0; kb < p.nk; ++kb) {
+                if (!mbar_wait(&bars->full[stage], phase, wc, kWhereMmaFull, t)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(a_tiles + stage * A_BYTES));
+                const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(b_tiles + stage * B_BYTES));
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, PIDESC, (kb | k) != 0 ? 1u : 0u);
+                umma_commit_pair_multicast(&bars->empty[stage], 0x3);
+                if (++stage == PSTAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit_pair_multicast(&bars->acc_full[acc], 0x3);
+        }
+        umma_commit_pair_multicast(&bars->drain, 0x1);
+        WaitCtx drain{p.status, &bars->abort_flag, p.wait_limit_ns};
+        int dummy_abort = 0;
+        drain.abort_flag = &dummy_abort;
+        mbar_wait(&bars->drain, 0, drain, kWhereDrain, -1);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const uint32_t acc_empty0 = mapa_shared(smem_u32(&bars->acc_empty[0]), 0);
+        const int quarter = warp & 3;
+        const int row_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
+        int local = 0;
+        for (int t = pair_id; t < total; t += npairs, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            const bool ok = mbar_wait(&bars->acc_full[acc], acc_phase, wc, kWhereEpilogueAccFull, t);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            int g, m, n;
+            decode_tile(p, t, g, m, n);
+            const int row = m * PBM + row_in_tile;
+            const bool row_ok = row < p.M;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[g]) + static_cast<long long>(row) * p.ldo;
+            if (EPI == Epi::kSwiGLU) {
+#pragma unroll 1
+                for (int c = 0; c < PBN / 2; c += 32) {
+                    uint32_t gv[32], uv[32];
+                    tmem_ld_32cols(taddr + c, gv);
+                    tmem_ld_32cols(taddr + PBN / 2 + c, uv);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
+                        const float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
+                        packed[j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
+                    }
+                    const int col = n * (PBN / 2) + c;
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (col + 8 * v < p.N)
+                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
+                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < PBN; c += 32) {
+                    uint32_t v32[32];
+                    tmem_ld_32cols(taddr + c, v32);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        packed[j] = pack_bf16x2(__uint_as_float(v32[2 * j]), __uint_as_float(v32[2 * j + 1]));
+                    const int col = n * PBN + c;
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (col + 8 * v < p.N)
+                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
+                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still touch its memory
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+}  // namespace pair
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
@@ -309,6 +550,52 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStre
         tc_gemm_kernel<Epi::kStore><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
     }
     return cudaGetLastError();
+}
+
+namespace {
+
+template <Epi EPI>
+cudaError_t launch_pair_typed(const TcGemmParams& p, int num_sms, cudaStream_t s) {
+    auto* kfn = pair::tc_gemm_pair_kernel<EPI>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::PSMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::PSMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many co-resident pairs as the GPU holds (one CTA per SM)
+    static int max_clusters[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int slot = (dev & 63);
+    if (max_clusters[slot] == 0) {
+        cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kfn, &cfg);
+        if (e != cudaSuccess || n <= 0) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+        max_clusters[slot] = n;
+    }
+    const int total = p.G * p.mt * p.nt;
+    const int pairs = total < max_clusters[slot] ? total : max_clusters[slot];
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, kfn, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm_pair(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s) {
+    if (p.G * p.mt * p.nt == 0) return cudaSuccess;
+    return epi == Epi::kSwiGLU ? launch_pair_typed<Epi::kSwiGLU>(p, num_sms, s)
+                               : launch_pair_typed<Epi::kStore>(p, num_sms, s);
 }
 
 }  // namespace sptp

@@ -4,9 +4,9 @@
 // the all-gather starting the next).  HBM-bound: every input byte is read
 // once with 128-bit coalesced loads, every output byte written once.
 //
-// One warp per token row.  Lane l owns the 16-byte column vectors
-// l, l+32, l+64, ... of the row and keeps h in fp32 registers, so the row
-// is read once; the sum of squares is reduced with warp shuffles.
+// A group of threads per token row, one 16-byte column vector per thread and
+// source, so every thread's loads are independent and in flight together; h
+// stays in fp32 registers, so the row is read once.
 // Summation order per element: r = ((0 + src_0) + src_1) + ... (fp32, list
 // order; no sources gives r = 0),
 // h = x + r; the norm uses the unrounded fp32 h.
@@ -76,38 +76,51 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Row fits in registers: NV vectors of E elements per lane.
-template <typename T, int NV>
-__global__ void __launch_bounds__(128) prologue_regs(const __grid_constant__ PrologueParams p) {
+// One group of `tpr` threads (a multiple of 32) per token row, R rows per CTA;
+// thread t of a group owns the 16-byte column vectors t, t+tpr, ... (VPT of
+// them), so each thread issues its (sources + 1) x VPT loads back to back.
+// The row's sum of squares is reduced with warp shuffles and, when a row
+// spans several warps, through a double-buffered shared array (one
+// __syncthreads per row).
+template <typename T, int VPT>
+__global__ void __launch_bounds__(1024) prologue_rows(const __grid_constant__ PrologueParams p, int tpr, int R) {
     using V = Vec<T>;
     constexpr int E = V::E;
+    extern __shared__ float red[];  // [2][R][tpr / 32]
+    const int grp = threadIdx.x / tpr;
+    const int t = threadIdx.x - grp * tpr;
     const int lane = threadIdx.x & 31;
-    const long long warps_total = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    const long long total_rows = static_cast<long long>(p.G) * p.M;
+    const int wpr = tpr >> 5;
+    const int wir = t >> 5;
+    const long long total = static_cast<long long>(p.G) * p.M;
     const int d = p.d;
-    for (long long gr = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < total_rows;
-         gr += warps_total) {
-        const int g = static_cast<int>(gr / p.M);
-        const long long row = gr - static_cast<long long>(g) * p.M;
-        const PrologueGroup& grp = p.grp[g];
-        const long long base = row * d;
-        float h[NV][E];
+    int parity = 0;
+    for (long long base = static_cast<long long>(blockIdx.x) * R; base < total;
+         base += static_cast<long long>(gridDim.x) * R) {
+        const long long gr = base + grp;
+        const bool active = gr < total;
+        const int g = active ? static_cast<int>(gr / p.M) : 0;
+        const long long row = active ? gr - static_cast<long long>(g) * p.M : 0;
+        const PrologueGroup& grpd = p.grp[g];
+        const long long off = row * d;
+        float h[VPT][E];
         float ss = 0.f;
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int col = (v * 32 + lane) * E;
-            if (col < d) {
+        for (int v = 0; v < VPT; ++v) {
+            const int col = (v * tpr + t) * E;
+            if (active && col < d) {
                 float r[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) r[e] = 0.f;
-                for (int s = 0; s < grp.n_src; ++s) {
-                    float t[E];
-                    V::load_stream(p.src[grp.src_begin + s], base + col, t);
+#pragma unroll 4
+                for (int s = 0; s < grpd.n_src; ++s) {
+                    float u[E];
+                    V::load_stream(p.src[grpd.src_begin + s], off + col, u);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) r[e] += t[e];
+                    for (int e = 0; e < E; ++e) r[e] += u[e];
                 }
                 float xv[E];
-                V::load_stream(grp.x, base + col, xv);
+                V::load_stream(grpd.x, off + col, xv);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     h[v][e] = xv[e] + r[e];
@@ -115,92 +128,32 @@ __global__ void __launch_bounds__(128) prologue_regs(const __grid_constant__ Pro
                 }
             }
         }
-        if (grp.h != nullptr) {
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                const int col = (v * 32 + lane) * E;
-                if (col < d) V::store(grp.h, base + col, h[v]);
-            }
+        ss = warp_sum(ss);
+        if (wpr > 1) {
+            float* slot = red + (parity * R + grp) * wpr;
+            if (lane == 0) slot[wir] = ss;
+            __syncthreads();
+            ss = 0.f;
+            for (int w = 0; w < wpr; ++w) ss += slot[w];
+            parity ^= 1;
         }
-        if (grp.y != nullptr) {
-            ss = warp_sum(ss);
-            const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
+        if (!active) continue;
+        const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
 #pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                const int col = (v * 32 + lane) * E;
-                if (col < d) {
+        for (int v = 0; v < VPT; ++v) {
+            const int col = (v * tpr + t) * E;
+            if (col < d) {
+                if (grpd.h != nullptr) V::store(grpd.h, off + col, h[v]);
+                if (grpd.y != nullptr) {
                     float gm[E];
                     V::load(p.gamma, col, gm);
 #pragma unroll
                     for (int e = 0; e < E; ++e) gm[e] = h[v][e] * inv * gm[e];
-                    V::store(grp.y, base + col, gm);
+                    V::store(grpd.y, off + col, gm);
                 }
             }
         }
     }
-}
-
-// Any d: two passes over the row (the second re-reads it from cache).
-template <typename T>
-__global__ void __launch_bounds__(128) prologue_two_pass(const __grid_constant__ PrologueParams p) {
-    using V = Vec<T>;
-    constexpr int E = V::E;
-    const int lane = threadIdx.x & 31;
-    const long long warps_total = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    const long long total_rows = static_cast<long long>(p.G) * p.M;
-    const int d = p.d;
-    for (long long gr = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < total_rows;
-         gr += warps_total) {
-        const int g = static_cast<int>(gr / p.M);
-        const long long row = gr - static_cast<long long>(g) * p.M;
-        const PrologueGroup& grp = p.grp[g];
-        const long long base = row * d;
-        float ss = 0.f;
-        for (int pass = 0; pass < 2; ++pass) {
-            float inv = 0.f;
-            if (pass == 1) {
-                if (grp.y == nullptr && grp.h == nullptr) break;
-                ss = warp_sum(ss);
-                inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
-            }
-            for (int col = lane * E; col < d; col += 32 * E) {
-                float r[E], h[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) r[e] = 0.f;
-                for (int s = 0; s < grp.n_src; ++s) {
-                    float t[E];
-                    V::load(p.src[grp.src_begin + s], base + col, t);
-#pragma unroll
-                    for (int e = 0; e < E; ++e) r[e] += t[e];
-                }
-                float xv[E];
-                V::load(grp.x, base + col, xv);
-#pragma unroll
-                for (int e = 0; e < E; ++e) h[e] = xv[e] + r[e];
-                if (pass == 0) {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) ss = fmaf(h[e], h[e], ss);
-                } else {
-                    // pass 1 reads x again, so h may alias x only after the
-                    // read of this vector (it is: same lane, same column)
-                    if (grp.y != nullptr) {
-                        float gm[E];
-                        V::load(p.gamma, col, gm);
-#pragma unroll
-                        for (int e = 0; e < E; ++e) gm[e] = h[e] * inv * gm[e];
-                        V::store(grp.y, base + col, gm);
-                    }
-                    if (grp.h != nullptr) V::store(grp.h, base + col, h);
-                }
-            }
-        }
-    }
-}
-
-template <typename T, int NV>
-cudaError_t launch_regs(const PrologueParams& p, int grid, cudaStream_t s) {
-    prologue_regs<T, NV><<<grid, 128, 0, s>>>(p);
-    return cudaGetLastError();
 }
 
 template <typename T>
@@ -208,18 +161,21 @@ cudaError_t launch_typed(const PrologueParams& p, int num_sms, cudaStream_t s) {
     constexpr int E = Vec<T>::E;
     const long long rows = static_cast<long long>(p.G) * p.M;
     if (rows == 0) return cudaSuccess;
-    long long grid = (rows + 3) / 4;  // 4 warps (rows) per block
-    const long long cap = static_cast<long long>(num_sms) * 16;
+    const int nvec = (p.d + E - 1) / E;
+    int vpt = 1;
+    while ((nvec + vpt - 1) / vpt > 1024) vpt *= 2;
+    if (vpt > 4) return cudaErrorInvalidValue;
+    const int tpr = (((nvec + vpt - 1) / vpt) + 31) / 32 * 32;
+    const int R = tpr >= 256 ? 1 : 256 / tpr;
+    const int block = tpr * R;
+    const size_t smem = static_cast<size_t>(2) * R * (tpr / 32) * sizeof(float);
+    long long grid = (rows + R - 1) / R;
+    const long long cap = static_cast<long long>(num_sms) * (2048 / block);
     if (grid > cap) grid = cap;
-    const int nv = (p.d + 32 * E - 1) / (32 * E);
     const int g = static_cast<int>(grid);
-    if (nv <= 1) return launch_regs<T, 1>(p, g, s);
-    if (nv <= 2) return launch_regs<T, 2>(p, g, s);
-    if (nv <= 4) return launch_regs<T, 4>(p, g, s);
-    if (nv <= 8) return launch_regs<T, 8>(p, g, s);
-    if (nv <= 12) return launch_regs<T, 12>(p, g, s);
-    if (nv <= 16) return launch_regs<T, 16>(p, g, s);
-    prologue_two_pass<T><<<g, 128, 0, s>>>(p);
+    if (vpt == 1) prologue_rows<T, 1><<<g, block, smem, s>>>(p, tpr, R);
+    else if (vpt == 2) prologue_rows<T, 2><<<g, block, smem, s>>>(p, tpr, R);
+    else prologue_rows<T, 4><<<g, block, smem, s>>>(p, tpr, R);
     return cudaGetLastError();
 }
 

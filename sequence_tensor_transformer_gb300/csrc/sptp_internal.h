@@ -77,6 +77,9 @@ struct TcGemmParams {
 enum class Epi { kSwiGLU, kStore };
 
 cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
+// CTA-pair (cta_group::2) variant: tiles of 256 rows (mt counts 256-row tiles)
+// and 256 B rows; same parameter block and tensor maps (boxes of 128 rows).
+cudaError_t launch_tc_gemm_pair(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
 size_t tc_gemm_smem_bytes();
 
 // Encodes a 2-D bf16 tensor map (inner = contiguous dim) with 128-byte swizzle.

@@ -23,6 +23,13 @@ def _lib():
     torch.cuda.set_device(0)
 
 
+@pytest.fixture(params=["pair", "single"])
+def gemm_variant(request, monkeypatch):
+    """Runs a test with the CTA-pair (default) and the single-CTA tcgen05 GEMMs."""
+    monkeypatch.setenv("SPTP_GEMM_VARIANT", request.param)
+    return request.param
+
+
 def case(M, d, F, P, C, dtype, down_from_F=True, seed=0):
     return synth.BoundaryConfig(f"t_{M}_{d}_{F}_{P}_{C}_{dtype}", M, d, F, P, C, dtype, down_from_F, seed=seed)
 
@@ -80,7 +87,7 @@ def test_prologue_matches_oracle(dtype, M, d, P):
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("M,d,F,P", [(64, 128, 512, 2), (300, 136, 400, 2), (257, 1024, 3 * 392, 3),
                                      (1024, 512, 2048, 4)])
-def test_gateup_swiglu_matches_oracle(dtype, M, d, F, P):
+def test_gateup_swiglu_matches_oracle(dtype, M, d, F, P, gemm_variant):
     rng = np.random.default_rng(F + M)
     y = synth._cast(rng.standard_normal((M, d)), dtype)
     W1g = synth._cast(rng.standard_normal((F, d)) / np.sqrt(d), dtype)
@@ -98,7 +105,7 @@ def test_gateup_swiglu_matches_oracle(dtype, M, d, F, P):
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("M,d,F,P", [(64, 128, 512, 2), (300, 136, 400, 2), (257, 1000, 3 * 392, 3),
                                      (1024, 512, 2048, 4)])
-def test_down_proj_matches_oracle(dtype, M, d, F, P):
+def test_down_proj_matches_oracle(dtype, M, d, F, P, gemm_variant):
     rng = np.random.default_rng(F + 3 * M)
     f = F // P
     s = synth._cast(rng.standard_normal((P, M, f)), dtype)
@@ -120,7 +127,7 @@ def test_tiny_fp32_config():
 
 @pytest.mark.parametrize("M,d,F,P,C", [(320, 256, 768, 2, 2), (384, 136, 3 * 200, 3, 3), (1000, 512, 4 * 392, 4, 8),
                                        (2048, 1024, 8 * 256, 8, 8), (130, 64, 64, 1, 1)])
-def test_boundary_bf16_multi_tile_and_ragged(M, d, F, P, C):
+def test_boundary_bf16_multi_tile_and_ragged(M, d, F, P, C, gemm_variant):
     check(*run_boundary(case(M, d, F, P, C, "bf16")), "bf16")
 
 
@@ -138,7 +145,7 @@ def sample_rows(M, n=24, seed=1):
     return sorted(set(base + list(rng.choice(M, n, replace=False))))
 
 
-def test_boundary_d4096_full_size_sampled_rows():
+def test_boundary_d4096_full_size_sampled_rows(gemm_variant):
     cfg = synth.BOUNDARY_D4096
     check(*run_boundary(cfg, rows=sample_rows(cfg.M)), "bf16")
 
