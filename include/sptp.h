@@ -56,7 +56,8 @@ typedef enum {
     SPTP_ERR_CUDA = -5,          /* a CUDA runtime call or kernel launch failed */
     SPTP_ERR_TIMEOUT = -6,       /* a bounded device-side wait ran out */
     SPTP_ERR_DEVICE = -7,        /* current device is not compute capability 10.3 */
-    SPTP_ERR_ALIAS = -8          /* an output overlaps an input it must not overlap */
+    SPTP_ERR_ALIAS = -8,         /* an output overlaps an input it must not overlap */
+    SPTP_ERR_TOO_LARGE = -9      /* the problem needs more scratch than the library's static array */
 } sptp_status;
 
 /* Bytes at the start of every workspace holding the device status words. */
@@ -175,6 +176,38 @@ int sptp_read_device_status(const void* workspace, void* cuda_stream);
  */
 int sptp_wait_selftest(void* workspace, size_t ws_bytes, unsigned long long limit_ns,
                        int preset_flag, void* cuda_stream);
+
+/* Bytes of the static device scratch array used by sptp_ffn_forward_noalloc. */
+#define SPTP_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * sptp_ffn_forward_noalloc -- sptp_ffn_forward for callers that cannot
+ * allocate device memory (for example a plugin inside a host framework that
+ * owns every device allocation, or a serving loop that must not call
+ * cudaMalloc because it can synchronise the device).  The pages describe no
+ * such entry point; it exists for those callers.
+ *   - Arguments, results and errors are those of sptp_ffn_forward, without
+ *     the workspace.  The caller still passes every input and output.
+ *   - Scratch is a library-owned 256-byte aligned __device__ array of
+ *     SPTP_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU loading the library
+ *     holds until the process exits.  Problems whose
+ *     sptp_ffn_workspace_size(...) exceeds it return SPTP_ERR_TOO_LARGE
+ *     before any CUDA call (bf16, d=4096, F=14336: up to about 1800 tokens).
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
+ *     call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array, so calls whose work overlaps on the
+ *     GPU (different streams, or different host threads) race and give wrong
+ *     results; serialise them.  The array keeps the last call's contents; the
+ *     status words are cleared at the start of each call.
+ *   - sptp_read_device_status does not apply (its status words live in the
+ *     shared array).
+ */
+int sptp_ffn_forward_noalloc(const void* x, const void* partials, const void* gamma,
+                             const void* W1g, const void* W1u, const void* W2,
+                             int M, int d, int F, int P, int chunks, float eps, int dtype,
+                             void* out, void* resid_out, void* cuda_stream);
 
 /* Human-readable text of a status code (static storage). */
 const char* sptp_status_string(int status);

@@ -17,17 +17,19 @@ __all__ = [
     "sptp_ffn_workspace_size", "sptp_ffn_forward", "dtp_ffn_stack_workspace_size",
     "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
     "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "EXPORTED_SYMBOLS",
+    "sptp_ffn_forward_noalloc", "SPTP_NOALLOC_SCRATCH_BYTES",
 ]
 
 SPTP_BF16 = 0
 SPTP_FP32 = 1
 SPTP_WS_HEADER_BYTES = 4096
+SPTP_NOALLOC_SCRATCH_BYTES = 64 << 20
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsptp.so")
 
 EXPORTED_SYMBOLS = (
     "sptp_ffn_workspace_size", "sptp_ffn_forward", "dtp_ffn_stack_workspace_size",
     "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
-    "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string",
+    "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "sptp_ffn_forward_noalloc",
 )
 
 _lib = None
@@ -44,6 +46,7 @@ _SIGS = {
     "sptp_read_device_status": (_I, [_P, _P]),
     "sptp_wait_selftest": (_I, [_P, _Z, _U64, _I, _P]),
     "sptp_status_string": (ctypes.c_char_p, [_I]),
+    "sptp_ffn_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
 }
 
 
@@ -192,6 +195,19 @@ def sptp_down_proj(s, W2, P, out=None, workspace=None, stream=None):
                                 workspace.numel(), _stream(stream))
     _check("sptp_down_proj", code)
     return out
+
+
+def sptp_ffn_forward_noalloc(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, out, resid_out=None,
+                             stream=None):
+    """SP-TP FFN boundary on the library's static scratch (no workspace and no
+    device allocation inside the call; the caller passes out/resid_out)."""
+    M, d = x.shape
+    F = W1g.shape[0]
+    code = lib().sptp_ffn_forward_noalloc(
+        _ptr(x), _ptr(partials), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, chunks, float(eps),
+        _dtype_code(x), _ptr(out), _ptr(resid_out), _stream(stream))
+    _check("sptp_ffn_forward_noalloc", code)
+    return out, resid_out
 
 
 def sptp_read_device_status(workspace, stream=None) -> int:

@@ -227,6 +227,7 @@ const char* sptp_status_string(int status) {
         case SPTP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
         case SPTP_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
         case SPTP_ERR_ALIAS: return "an output overlaps an input";
+        case SPTP_ERR_TOO_LARGE: return "problem needs more scratch than the static no-allocation array holds";
         default: return "unknown status";
     }
 }
