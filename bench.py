@@ -188,10 +188,15 @@ def cores() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(cfg, rows=512):
-    f = oracle_inputs(cfg, rows)
-    oracle_rate(cfg, 8, {k: (v[:8] if k == "x" else v[:, :8] if k == "partials" else v) for k, v in f.items()})
-    sec = oracle_rate(cfg, rows, f)
+def cpu_baseline(cfg, target_s=10.0):
+    """The oracle on the first rows of the workload, sized for ~target_s of
+    host work (at most the whole workload)."""
+    full = oracle_inputs(cfg, cfg.M)
+    sub = lambda r: {k: (v[:r] if k == "x" else v[:, :r] if k == "partials" else v) for k, v in full.items()}
+    probe = min(256, cfg.M)
+    t = oracle_rate(cfg, probe, sub(probe))
+    rows = int(min(cfg.M, max(probe, target_s / max(t / probe, 1e-9))))
+    sec = oracle_rate(cfg, rows, sub(rows))
     tflops = 6.0 * rows * cfg.d * cfg.F / sec / 1e12
     return {"value": tflops, "unit": UNIT, "tokens_per_s": rows / sec, "cores": cores(), "kind": "oracle",
             "sample": f"first {rows} of {cfg.M} token rows of the workload (rows are independent), float64 numpy "
@@ -247,10 +252,20 @@ def kernel_traffic(kernel: str):
     j = json.load(open(path)).get(kernel)
     if not j:
         return None
-    src = os.path.join(ROOT, "sequence_tensor_transformer_gb300", "csrc", j["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != j["source_sha"]:
+    if not isinstance(j, dict) or "sources" not in j or sources_sha(j["sources"]) != j.get("sources_sha"):
         return None
     return j["bytes_per_launch"]
+
+
+def sources_sha(names) -> str:
+    """Hash of the kernel source and the launch code the counters depend on."""
+    h = hashlib.sha256()
+    for n in names:
+        path = os.path.join(ROOT, "sequence_tensor_transformer_gb300", "csrc", n)
+        if not os.path.exists(path):
+            return ""
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def run_ours(args):

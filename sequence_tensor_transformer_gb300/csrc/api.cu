@@ -203,13 +203,18 @@ int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype
     return cuda_status(launch_simt_gemm(p, Epi::kStore, s));
 }
 
-// Raster band (m-tiles walked together) from the sequence chunk height.
+// Raster band: the GEMMs walk the m-tiles of 4096 rows (or of one sequence
+// chunk, if taller) against each B panel before moving to the next panel, so
+// the band's A tiles stay in L2 while the weights are streamed about M/4096
+// times.  (Measured on the 8192 x 4096 x 14336 boundary, end to end: bands of
+// 1024 / 2048 / 4096 / 8192 rows gave 1589 / 1644 / 1658 / 1602 TFLOP/s.)
+constexpr int kBandRows = 4096;
+
 int band_for_chunks(int M, int chunks) {
-    const int rows = chunks > 0 ? M / chunks : M;
-    int band = rows / kBM;
-    if (band < 1 || rows % kBM != 0) band = 8;
-    if (band > 16) band = 16;
-    return band;
+    const int chunk_rows = chunks > 0 ? M / chunks : M;
+    const int rows = chunk_rows > kBandRows ? chunk_rows : kBandRows;
+    const int band = rows / kBM;
+    return band < 1 ? 1 : band;
 }
 
 }  // namespace
@@ -293,6 +298,8 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
     pp.gamma = gamma;
     pp.grp[0] = PrologueGroup{x, resid_out, y, 0, P};
     for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
+    pp.status = ws_status(workspace);
+    pp.wait_limit_ns = kWaitLimitNs;
     if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
 
     // 4-6: chunked gather (identity) + column-parallel gate/up + SwiGLU,
@@ -382,17 +389,19 @@ int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, co
                         if (q != p) pp.src[ns++] = o(kk, q);
             pp.grp[p] = PrologueGroup{xs(p), xs(p), l < L ? yp(p) : nullptr, begin, ns - begin};
         }
+        pp.status = ws_status(workspace);
+        pp.wait_limit_ns = kWaitLimitNs;
         if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
         if (l == L) break;
 
         const size_t woff = static_cast<size_t>(l) * F * d * es;
         for (int p = 0; p < P; ++p) A[p] = yp(p);
-        if ((rc = gateup(A, cptr(W1g, woff), cptr(W1u, woff), M, d, F, P, dtype, sbuf, ws_status(workspace), 8,
-                         di, s)) != SPTP_OK)
+        if ((rc = gateup(A, cptr(W1g, woff), cptr(W1u, woff), M, d, F, P, dtype, sbuf, ws_status(workspace),
+                         band_for_chunks(M, 1), di, s)) != SPTP_OK)
             return rc;
         for (int p = 0; p < P; ++p) outs[p] = o(l, p);
-        if ((rc = down(sbuf, cptr(W2, woff), M, d, F, P, dtype, outs, ws_status(workspace), 8, di, s)) !=
-            SPTP_OK)
+        if ((rc = down(sbuf, cptr(W2, woff), M, d, F, P, dtype, outs, ws_status(workspace), band_for_chunks(M, 1),
+                       di, s)) != SPTP_OK)
             return rc;
         (void)f;
     }
@@ -428,6 +437,8 @@ int sptp_prologue(const void* x, const void* partials, const void* gamma, int M,
     pp.gamma = gamma;
     pp.grp[0] = PrologueGroup{x, h_out, y_out, 0, P};
     for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
+    pp.status = nullptr;  // no workspace: a timed-out wait only stops the CTA
+    pp.wait_limit_ns = kWaitLimitNs;
     return cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -452,7 +463,7 @@ int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u, int M, i
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     const void* A[kMaxGroups];
     for (int g = 0; g < P; ++g) A[g] = y;
-    return gateup(A, W1g, W1u, M, d, F, P, dtype, s_out, ws_status(workspace), 8, di, s);
+    return gateup(A, W1g, W1u, M, d, F, P, dtype, s_out, ws_status(workspace), band_for_chunks(M, 1), di, s);
 }
 
 int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype, void* out,
@@ -477,7 +488,7 @@ int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P,
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     void* outs[kMaxGroups];
     for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * M * d * es);
-    return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), 8, di, s);
+    return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), band_for_chunks(M, 1), di, s);
 }
 
 int sptp_read_device_status(const void* workspace, void* cuda_stream) {

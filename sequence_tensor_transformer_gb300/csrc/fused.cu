@@ -1,0 +1,448 @@
+// Fused persistent SP-TP FFN boundary ("[Feature] Async Tensor Parallelism for
+// Archon Engine", "Potential Solution": decompose all-gather + matmul into
+// chunked pipelined operations, and overlap the sub-layer boundary's residual
+// add + RMSNorm with the matmuls).
+//
+// One launch of CTA pairs (cta_group::2, one CTA per SM, all co-resident)
+// computes the whole boundary:
+//   warps 6..9   prologue: rows r = w, w + W, ... (W prologue warps in the
+//                grid) in sequence order: h = x + sum_p partials[p], y =
+//                RMSNorm(h) * gamma; after each row a release increment of
+//                the row's 256-row block counter (rows become "gathered" as
+//                soon as they are produced)
+//   warp 0       TMA producer: before a gate/up tile's first A load it waits
+//                (bounded) until the tile's 256 rows of y are ready; before a
+//                down tile's, until every gate/up tile of its (shard, rows)
+//                has been stored
+//   warp 1       MMA issuer of the even CTA (M=256, N=256, K=16 UMMAs)
+//   warps 2..5   epilogue: SwiGLU into s (then a release increment of the
+//                (shard, 256-row block) counter) or the bf16 partials out
+// The tile sequence is all gate/up tiles (raster bands of `band` 256-row
+// tiles), then all down tiles; pair q takes tiles q, q + npairs, ...  Every
+// dependency points to work earlier in that order or to prologue rows, which
+// never wait, so with all CTAs resident every wait ends.
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "sptp_ptx.cuh"
+
+namespace sptp {
+
+namespace {
+
+constexpr int BK = 64;
+constexpr int PBM = 256, PBN = 256;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 128 * BK * 2;
+constexpr int B_BYTES = 128 * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int PRO_WARPS = 4;
+constexpr int THREADS = 32 * (6 + PRO_WARPS);
+constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN);
+
+struct Bars {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block too large");
+
+struct Tile {
+    bool down;
+    int g, m, n;
+};
+
+__device__ __forceinline__ Tile decode(const FusedParams& p, int t) {
+    Tile r;
+    r.down = t >= p.tiles_gu;
+    const int nt = r.down ? p.nt_dn : p.nt_gu;
+    if (r.down) t -= p.tiles_gu;
+    const int per_band = p.band * p.P * nt;
+    const int b = t / per_band;
+    const int rr = t - b * per_band;
+    const int m0 = b * p.band;
+    const int bm = min(p.band, p.mt - m0);
+    r.m = m0 + rr % bm;
+    const int gn = rr / bm;
+    r.g = gn / nt;
+    r.n = gn - r.g * nt;
+    return r;
+}
+
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_release_add(int* ctr, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 v = __bfloat1622float2(h2[i]);
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 u;
+    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return u;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// h = x + (0 + partial_0 + partial_1 + ...) for 8 columns of one row
+__device__ __forceinline__ void row_h8(const FusedParams& p, long long off, float (&h)[8]) {
+    float r[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) r[e] = 0.f;
+    for (int q = 0; q < p.P; ++q) {
+        float u[8];
+        load8(static_cast<const __nv_bfloat16*>(p.partials[q]) + off, u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r[e] += u[e];
+    }
+    load8(static_cast<const __nv_bfloat16*>(p.x) + off, h);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[e] += r[e];
+}
+
+__global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid_constant__ FusedParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t* a_tiles = smem;
+    uint8_t* b_tiles = smem + STAGES * A_BYTES;
+    Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars->acc_full[a], 1);
+            mbar_init(&bars->acc_empty[a], 2 * 4 * 32);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.mapY);
+        for (int g = 0; g < p.P; ++g) {
+            tma_prefetch_map(&p.mapW1g[g]);
+            tma_prefetch_map(&p.mapW1u[g]);
+            tma_prefetch_map(&p.mapS[g]);
+            tma_prefetch_map(&p.mapW2[g]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    WaitCtx wc{p.status, &bars->abort_flag, p.wait_limit_ns};
+    const int total = p.tiles_gu + p.tiles_dn;
+    const int pair_id = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (warp >= 6) {
+        // ------------------------------------------------ prologue rows
+        const int W = gridDim.x * PRO_WARPS;
+        const int d = p.d;
+        for (long long row = static_cast<long long>(blockIdx.x) * PRO_WARPS + (warp - 6); row < p.M; row += W) {
+            if (*wc.abort_flag) break;
+            const long long base = row * d;
+            float ss = 0.f;
+            for (int col = lane * 8; col < d; col += 256) {
+                float h[8];
+                row_h8(p, base + col, h);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(h[e], h[e], ss);
+            }
+            ss = warp_sum(ss);
+            const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
+            for (int col = lane * 8; col < d; col += 256) {
+                float h[8], gm[8];
+                row_h8(p, base + col, h);  // same inputs and order: the same h
+                load8(static_cast<const __nv_bfloat16*>(p.gamma) + col, gm);
+                if (p.h_out != nullptr) __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.h_out) + base + col), pack8(h));
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gm[e] = h[e] * inv * gm[e];
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + base + col) = pack8(gm);
+            }
+            // make the row's y visible to the TMA loads of other CTAs
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) red_release_add(&p.rb_ready[row >> 8], 1);
+        }
+    } else if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        const uint32_t full0 = mapa_shared(smem_u32(&bars->full[0]), 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        int armed_parity[STAGES];
+        for (int s = 0; s < STAGES; ++s) armed_parity[s] = -1;
+        bool ok = true;
+        for (int t = pair_id; ok && t < total; t += npairs) {
+            const Tile tl = decode(p, t);
+            // dependency of this tile's A operand
+            if (!tl.down) {
+                const int need = min(PBM, p.M - tl.m * PBM);
+                ok = flag_wait_geq(&p.rb_ready[tl.m], need, wc, kWhereFusedRows, t);
+            } else {
+                ok = flag_wait_geq(&p.gu_done[tl.g * p.mt + tl.m], 2 * p.nt_gu, wc, kWhereFusedGateUp, t);
+            }
+            if (!ok) break;
+            fence_proxy_async_global();
+            const int nk = tl.down ? p.nk_dn : p.nk_gu;
+            const CUtensorMap* mA = tl.down ? &p.mapS[tl.g] : &p.mapY;
+            const CUtensorMap* mB = tl.down ? &p.mapW2[tl.g] : (rank == 0 ? &p.mapW1g[tl.g] : &p.mapW1u[tl.g]);
+            const int brow = tl.down ? tl.n * PBN + static_cast<int>(rank) * 128 : tl.n * 128;
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!mbar_wait(&bars->empty[stage], phase ^ 1u, wc, kWhereProducerEmpty, t)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    mbar_arrive_expect_tx(&bars->full[stage], 2 * STAGE_BYTES);
+                    armed_parity[stage] = static_cast<int>(phase);
+                }
+                const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+                tma_load_2d_pair(a_tiles + stage * A_BYTES, mA, fb, kb * BK, tl.m * PBM + static_cast<int>(rank) * 128);
+                tma_load_2d_pair(b_tiles + stage * B_BYTES, mB, fb, kb * BK, brow);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        WaitCtx drain{p.status, &bars->abort_flag, p.wait_limit_ns};
+        int dummy_abort = 0;
+        drain.abort_flag = &dummy_abort;
+        if (leader) {
+            for (int s = 0; s < STAGES; ++s)
+                if (armed_parity[s] >= 0)
+                    mbar_wait(&bars->full[s], static_cast<uint32_t>(armed_parity[s]), drain, kWhereDrain, s);
+        } else if (!ok) {
+            const unsigned long long t0 = global_timer_ns();
+            while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        int local = 0;
+        for (int t = pair_id; ok && t < total; t += npairs, ++local) {
+            const Tile tl = decode(p, t);
+            const int nk = tl.down ? p.nk_dn : p.nk_gu;
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, wc, kWhereMmaAccEmpty, t)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PBN);
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!mbar_wait(&bars->full[stage], phase, wc, kWhereMmaFull, t)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(a_tiles + stage * A_BYTES));
+                const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(b_tiles + stage * B_BYTES));
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, IDESC, (kb | k) != 0 ? 1u : 0u);
+                umma_commit_pair_multicast(&bars->empty[stage], 0x3);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit_pair_multicast(&bars->acc_full[acc], 0x3);
+        }
+        umma_commit_pair_multicast(&bars->drain, 0x1);
+        WaitCtx drain{p.status, &bars->abort_flag, p.wait_limit_ns};
+        int dummy_abort = 0;
+        drain.abort_flag = &dummy_abort;
+        mbar_wait(&bars->drain, 0, drain, kWhereDrain, -1);
+    } else if (warp >= 2 && warp < 6) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const uint32_t acc_empty0 = mapa_shared(smem_u32(&bars->acc_empty[0]), 0);
+        const int quarter = warp & 3;
+        const int row_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
+        int local = 0;
+        for (int t = pair_id; t < total; t += npairs, ++local) {
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            const bool ok = mbar_wait(&bars->acc_full[acc], acc_phase, wc, kWhereEpilogueAccFull, t);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const Tile tl = decode(p, t);
+            const int row = tl.m * PBM + row_in_tile;
+            const bool row_ok = row < p.M;
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
+            if (!tl.down) {
+                __nv_bfloat16* out =
+                    reinterpret_cast<__nv_bfloat16*>(p.s_out[tl.g]) + static_cast<long long>(row) * p.f;
+#pragma unroll 1
+                for (int c = 0; c < PBN / 2; c += 32) {
+                    uint32_t gv[32], uv[32];
+                    tmem_ld_32cols(taddr + c, gv);
+                    tmem_ld_32cols(taddr + PBN / 2 + c, uv);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
+                        const float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
+                        packed[j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
+                    }
+                    const int col = tl.n * (PBN / 2) + c;
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (col + 8 * v < p.f)
+                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
+                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    }
+                }
+            } else {
+                __nv_bfloat16* out =
+                    reinterpret_cast<__nv_bfloat16*>(p.out[tl.g]) + static_cast<long long>(row) * p.d;
+#pragma unroll 1
+                for (int c = 0; c < PBN; c += 32) {
+                    uint32_t v32[32];
+                    tmem_ld_32cols(taddr + c, v32);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        packed[j] = pack_bf16x2(__uint_as_float(v32[2 * j]), __uint_as_float(v32[2 * j + 1]));
+                    const int col = tl.n * PBN + c;
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            if (col + 8 * v < p.d)
+                                __stcs(reinterpret_cast<uint4*>(out + col + 8 * v),
+                                       make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+            if (!tl.down) {
+                // this CTA's 128 rows of the s tile are stored: publish them
+                // to the down tiles' TMA loads
+                fence_proxy_async_global();
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (warp == 2 && lane == 0) red_release_add(&p.gu_done[tl.g * p.mt + tl.m], 1);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
+}  // namespace
+
+// Number of co-resident CTA pairs of the fused kernel (0 if it cannot run).
+int fused_max_pairs(int num_sms) {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int slot = dev & 63;
+    if (cached[slot] != 0) return cached[slot] < 0 ? 0 : cached[slot];
+    if (cudaFuncSetAttribute(boundary_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+        cudaSuccess) {
+        cached[slot] = -1;
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, boundary_fused_kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        cached[slot] = -1;
+        return 0;
+    }
+    cached[slot] = n;
+    return n;
+}
+
+cudaError_t launch_boundary_fused(const FusedParams& p, int pairs, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(boundary_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // the CTAs wait on one another's work: all of them must be resident
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, boundary_fused_kernel, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace sptp

@@ -480,11 +480,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                         packed[j] = pack_bf16x2(__uint_as_float(v32[2 * j]), __uint_as_float(v32[2 * j + 1]));
                     const int col = n * PBN + c;
                     if (row_ok) {
+                        // the partials are final outputs: evict-first stores
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             if (col + 8 * v < p.N)
-                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
-                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                                __stcs(reinterpret_cast<uint4*>(out + col + 8 * v),
+                                       make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
                     }
                 }
             }

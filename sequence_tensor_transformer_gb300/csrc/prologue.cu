@@ -12,7 +12,7 @@
 // h = x + r; the norm uses the unrounded fp32 h.
 #include <cuda_bf16.h>
 
-#include "sptp_internal.h"
+#include "sptp_ptx.cuh"
 
 namespace sptp {
 
@@ -45,12 +45,30 @@ struct Vec<__nv_bfloat16> {
             f[2 * i + 1] = v.y;
         }
     }
+    __device__ static void load_smem(const uint8_t* base, int idx, float (&f)[8]) {
+        const uint4 u = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(idx) * 2);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 v = __bfloat1622float2(h2[i]);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    }
     __device__ static void store(void* base, long long idx, const float (&f)[8]) {
         uint4 u;
         __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
         for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
         *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + idx) = u;
+    }
+    // evict-first store (final outputs nobody reads next)
+    __device__ static void store_stream(void* base, long long idx, const float (&f)[8]) {
+        uint4 u;
+        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + idx), u);
     }
 };
 
@@ -65,8 +83,15 @@ struct Vec<float> {
         const float4 v = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx));
         f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
     }
+    __device__ static void load_smem(const uint8_t* base, int idx, float (&f)[4]) {
+        const float4 v = *reinterpret_cast<const float4*>(base + static_cast<size_t>(idx) * 4);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
     __device__ static void store(void* base, long long idx, const float (&f)[4]) {
         *reinterpret_cast<float4*>(static_cast<float*>(base) + idx) = make_float4(f[0], f[1], f[2], f[3]);
+    }
+    __device__ static void store_stream(void* base, long long idx, const float (&f)[4]) {
+        __stcs(reinterpret_cast<float4*>(static_cast<float*>(base) + idx), make_float4(f[0], f[1], f[2], f[3]));
     }
 };
 
@@ -156,16 +181,198 @@ __global__ void __launch_bounds__(1024) prologue_rows(const __grid_constant__ Pr
     }
 }
 
+// Rows streamed through shared memory: thread 0 bulk-copies the (sources +
+// 1) input rows of the CTA's next rows into an S-stage ring (one mbarrier per
+// stage); the CTA's threads reduce the row from shared memory (VPT 16-byte
+// vectors each, gamma held in registers) and store h and y with coalesced
+// 16-byte stores (h, a final output, with evict-first hints; y stays in L2
+// for the gate/up GEMM).  One __syncthreads per row: it completes the row's
+// sum of squares and frees the row's stage, which thread 0 then refills with
+// the row S ahead.  A CTA handles rows blockIdx.x, blockIdx.x + gridDim.x, ...
+constexpr int kTmaMaxStages = 8;
+
+struct TmaLayout {
+    int S;              // stages
+    int max_src;        // sources per stage slot (max over groups)
+    uint32_t row_bytes; // d * sizeof(T)
+};
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ PrologueParams p, TmaLayout L) {
+    using V = Vec<T>;
+    constexpr int E = V::E;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    __shared__ uint64_t full[kTmaMaxStages];
+    __shared__ float red[2][16];
+    __shared__ int abort_flag;
+    const int nthr = blockDim.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const long long total = static_cast<long long>(p.G) * p.M;
+    const int d = p.d;
+    const uint32_t slot_bytes = L.row_bytes;
+    const uint32_t stage_bytes = slot_bytes * static_cast<uint32_t>(L.max_src + 1);
+    const long long first = blockIdx.x, stride = gridDim.x;
+    const long long my_rows = first < total ? (total - first + stride - 1) / stride : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < L.S; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // thread 0: start the copies of this CTA's i-th row into stage i % S
+    auto issue = [&](long long i) {
+        const long long gr = first + i * stride;
+        const int g = static_cast<int>(gr / p.M);
+        const long long row = gr - static_cast<long long>(g) * p.M;
+        const PrologueGroup& grp = p.grp[g];
+        const int s = static_cast<int>(i % L.S);
+        uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], slot_bytes * static_cast<uint32_t>(grp.n_src + 1));
+        const long long off = row * static_cast<long long>(slot_bytes);
+        bulk_load(st, static_cast<const uint8_t*>(grp.x) + off, slot_bytes, &full[s]);
+        for (int j = 0; j < grp.n_src; ++j)
+            bulk_load(st + static_cast<size_t>(j + 1) * slot_bytes,
+                      static_cast<const uint8_t*>(p.src[grp.src_begin + j]) + off, slot_bytes, &full[s]);
+    };
+    if (tid == 0)
+        for (long long i = 0; i < L.S && i < my_rows; ++i) issue(i);
+
+    float gm[VPT][E];
+    if (p.gamma != nullptr) {
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int col = (v * nthr + tid) * E;
+            if (col < d) V::load(p.gamma, col, gm[v]);
+        }
+    }
+
+    WaitCtx wc{p.status, &abort_flag, p.wait_limit_ns};
+    int parity = 0;
+    long long i = 0;
+    for (; i < my_rows; ++i) {
+        const int s = static_cast<int>(i % L.S);
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / L.S) & 1), wc, kWherePrologueFull,
+                                  static_cast<int>(i));
+        const long long gr = first + i * stride;
+        const int g = static_cast<int>(gr / p.M);
+        const long long row = gr - static_cast<long long>(g) * p.M;
+        const PrologueGroup& grp = p.grp[g];
+        const uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+        float h[VPT][E];
+        float ss = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int col = (v * nthr + tid) * E;
+                if (col < d) {
+                    float r[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) r[e] = 0.f;
+                    for (int j = 0; j < grp.n_src; ++j) {
+                        float u[E];
+                        V::load_smem(st + static_cast<size_t>(j + 1) * slot_bytes, col, u);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) r[e] += u[e];
+                    }
+                    float xv[E];
+                    V::load_smem(st, col, xv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        h[v][e] = xv[e] + r[e];
+                        ss = fmaf(h[v][e], h[v][e], ss);
+                    }
+                }
+            }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) red[parity][warp] = ss;
+        __syncthreads();
+        if (abort_flag) break;  // uniform: written before the barrier
+        if (tid == 0 && i + L.S < my_rows) {
+            // every thread has read stage s; order those reads before the
+            // copies that overwrite it
+            fence_proxy_async_smem();
+            issue(i + L.S);
+        }
+        ss = 0.f;
+        for (int w = 0; w < nwarps; ++w) ss += red[parity][w];
+        parity ^= 1;
+        const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
+        const long long off = row * d;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int col = (v * nthr + tid) * E;
+            if (col < d) {
+                if (grp.h != nullptr) V::store_stream(grp.h, off + col, h[v]);
+                if (grp.y != nullptr) {
+                    float yv[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) yv[e] = h[v][e] * inv * gm[v][e];
+                    V::store(grp.y, off + col, yv);
+                }
+            }
+        }
+    }
+    if (i < my_rows && tid == 0) {
+        // left early: wait (bounded) for copies still in flight into the ring
+        int local_abort = 0;
+        WaitCtx drain{p.status, &local_abort, p.wait_limit_ns};
+        for (long long j = i; j < my_rows && j < i + L.S; ++j)
+            mbar_wait(&full[j % L.S], static_cast<uint32_t>((j / L.S) & 1), drain, kWhereDrain, -1);
+    }
+}
+
+template <typename T, int VPT>
+cudaError_t launch_tma(const PrologueParams& p, const TmaLayout& L, int threads, int num_sms, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(L.S) * L.row_bytes * (L.max_src + 1) + 128;
+    cudaError_t e = cudaFuncSetAttribute(prologue_tma<T, VPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const long long rows = static_cast<long long>(p.G) * p.M;
+    int per_sm = static_cast<int>((200u * 1024u) / smem);
+    const int by_threads = 2048 / threads;
+    if (per_sm > by_threads) per_sm = by_threads;
+    if (per_sm > 8) per_sm = 8;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = static_cast<long long>(num_sms) * per_sm;
+    if (grid > rows) grid = rows;
+    prologue_tma<T, VPT><<<static_cast<int>(grid), threads, smem, s>>>(p, L);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_typed(const PrologueParams& p, int num_sms, cudaStream_t s) {
     constexpr int E = Vec<T>::E;
     const long long rows = static_cast<long long>(p.G) * p.M;
     if (rows == 0) return cudaSuccess;
     const int nvec = (p.d + E - 1) / E;
-    int vpt = 1;
-    while ((nvec + vpt - 1) / vpt > 1024) vpt *= 2;
-    if (vpt > 4) return cudaErrorInvalidValue;
-    const int tpr = (((nvec + vpt - 1) / vpt) + 31) / 32 * 32;
+
+    // Shared-memory streaming path: rows of all sources staged by bulk copies.
+    int max_src = 0;
+    for (int g = 0; g < p.G; ++g) max_src = p.grp[g].n_src > max_src ? p.grp[g].n_src : max_src;
+    const size_t stage_bytes = static_cast<size_t>(p.d) * sizeof(T) * (max_src + 1);
+    int S = static_cast<int>((96u * 1024u) / stage_bytes);
+    if (S > 4) S = 4;
+    if (S < 2 && 2 * stage_bytes <= 200u * 1024u) S = 2;
+    // up to 512 threads, one 16-byte vector each per source when it fits
+    const int threads = nvec <= 512 ? (nvec + 31) / 32 * 32 : 512;
+    const int vpt = (nvec + threads - 1) / threads;
+    if (S >= 2 && vpt <= 8) {
+        TmaLayout L{S, max_src, static_cast<uint32_t>(p.d * sizeof(T))};
+        if (vpt <= 1) return launch_tma<T, 1>(p, L, threads, num_sms, s);
+        if (vpt <= 2) return launch_tma<T, 2>(p, L, threads, num_sms, s);
+        if (vpt <= 4) return launch_tma<T, 4>(p, L, threads, num_sms, s);
+        return launch_tma<T, 8>(p, L, threads, num_sms, s);
+    }
+
+    // Register path (rows too wide for the shared-memory ring).
+    int vptr = 1;
+    while ((nvec + vptr - 1) / vptr > 1024) vptr *= 2;
+    if (vptr > 4) return cudaErrorInvalidValue;
+    const int tpr = (((nvec + vptr - 1) / vptr) + 31) / 32 * 32;
     const int R = tpr >= 256 ? 1 : 256 / tpr;
     const int block = tpr * R;
     const size_t smem = static_cast<size_t>(2) * R * (tpr / 32) * sizeof(float);
@@ -173,8 +380,8 @@ cudaError_t launch_typed(const PrologueParams& p, int num_sms, cudaStream_t s) {
     const long long cap = static_cast<long long>(num_sms) * (2048 / block);
     if (grid > cap) grid = cap;
     const int g = static_cast<int>(grid);
-    if (vpt == 1) prologue_rows<T, 1><<<g, block, smem, s>>>(p, tpr, R);
-    else if (vpt == 2) prologue_rows<T, 2><<<g, block, smem, s>>>(p, tpr, R);
+    if (vptr == 1) prologue_rows<T, 1><<<g, block, smem, s>>>(p, tpr, R);
+    else if (vptr == 2) prologue_rows<T, 2><<<g, block, smem, s>>>(p, tpr, R);
     else prologue_rows<T, 4><<<g, block, smem, s>>>(p, tpr, R);
     return cudaGetLastError();
 }

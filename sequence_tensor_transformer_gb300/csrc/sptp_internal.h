@@ -30,6 +30,8 @@ enum : int {
     kWhereDrain = 5,
     kWhereSelftestFlag = 6,
     kWhereSelftestBarrier = 7,
+    kWherePrologueFull = 8,
+    kWherePrologueEmpty = 9,
 };
 
 // Default limit of every bounded device-side wait (ns). A legitimate wait in
@@ -51,6 +53,8 @@ struct PrologueParams {
     const void* gamma;   // [d]
     int G, M, d;
     float eps;
+    DeviceStatus* status;            // may be null (no status words)
+    unsigned long long wait_limit_ns;
 };
 
 // Launches the partial-sum + residual + RMSNorm kernel over G groups of M rows.
