@@ -5,7 +5,7 @@
 //
 // One launch of CTA pairs (cta_group::2, one CTA per SM, all co-resident)
 // computes the whole boundary:
-//   warps 6..9   prologue: rows r = w, w + W, ... (W prologue warps in the
+//   warps 6..13  prologue: rows r = w, w + W, ... (W prologue warps in the
 //                grid) in sequence order: h = x + sum_p partials[p], y =
 //                RMSNorm(h) * gamma; after each row a release increment of
 //                the row's 256-row block counter (rows become "gathered" as
@@ -39,7 +39,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 constexpr int TMEM_COLS = 512;
-constexpr int PRO_WARPS = 4;
+constexpr int PRO_WARPS = 8;
 constexpr int THREADS = 32 * (6 + PRO_WARPS);
 constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN);
 
@@ -59,15 +59,33 @@ struct Tile {
     int g, m, n;
 };
 
+// Tile t of the sequence.  Gate/up tiles: a first raster band of band0
+// m-tiles (one sequence chunk, so the first wave waits only for that chunk's
+// rows), then bands of `band`; down tiles: bands of `band`.  Inside a band the
+// m-tile index runs fastest.
 __device__ __forceinline__ Tile decode(const FusedParams& p, int t) {
     Tile r;
     r.down = t >= p.tiles_gu;
     const int nt = r.down ? p.nt_dn : p.nt_gu;
-    if (r.down) t -= p.tiles_gu;
+    int m0 = 0;
+    if (r.down) {
+        t -= p.tiles_gu;
+    } else {
+        const int first = p.band0 * p.P * nt;
+        if (t < first) {
+            r.m = t % p.band0;
+            const int gn = t / p.band0;
+            r.g = gn / nt;
+            r.n = gn - r.g * nt;
+            return r;
+        }
+        t -= first;
+        m0 = p.band0;
+    }
     const int per_band = p.band * p.P * nt;
     const int b = t / per_band;
     const int rr = t - b * per_band;
-    const int m0 = b * p.band;
+    m0 += b * p.band;
     const int bm = min(p.band, p.mt - m0);
     r.m = m0 + rr % bm;
     const int gn = rr / bm;
@@ -89,6 +107,20 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 __device__ __forceinline__ void red_release_add(int* ctr, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+// OR of `v` over the 128 epilogue threads (named barrier 1).
+__device__ __forceinline__ bool epilogue_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.or.pred pout, 1, 128, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
@@ -116,20 +148,44 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// h = x + (0 + partial_0 + partial_1 + ...) for 8 columns of one row
-__device__ __forceinline__ void row_h8(const FusedParams& p, long long off, float (&h)[8]) {
-    float r[8];
+// h = x + (0 + partial_0 + partial_1 + ...) for NV 8-column vectors of one
+// row, 256 columns apart (vectors past d are left untouched); the loads of
+// one source for all NV vectors are issued together.
+template <int NV>
+__device__ __forceinline__ void row_h(const FusedParams& p, long long row_off, int col0, float (&h)[NV][8]) {
+    float r[NV][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) r[e] = 0.f;
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r[v][e] = 0.f;
     for (int q = 0; q < p.P; ++q) {
-        float u[8];
-        load8(static_cast<const __nv_bfloat16*>(p.partials[q]) + off, u);
+        uint4 u[NV];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) r[e] += u[e];
+        for (int v = 0; v < NV; ++v)
+            if (col0 + 256 * v < p.d)
+                u[v] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.partials[q]) +
+                                                            row_off + col0 + 256 * v));
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            if (col0 + 256 * v < p.d) {
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[v]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f2 = __bfloat1622float2(h2[i]);
+                    r[v][2 * i] += f2.x;
+                    r[v][2 * i + 1] += f2.y;
+                }
+            }
+        }
     }
-    load8(static_cast<const __nv_bfloat16*>(p.x) + off, h);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) h[e] += r[e];
+    for (int v = 0; v < NV; ++v) {
+        if (col0 + 256 * v < p.d) {
+            load8(static_cast<const __nv_bfloat16*>(p.x) + row_off + col0 + 256 * v, h[v]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) h[v][e] += r[v][e];
+        }
+    }
 }
 
 __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid_constant__ FusedParams p) {
@@ -189,23 +245,36 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
         for (long long row = static_cast<long long>(blockIdx.x) * PRO_WARPS + (warp - 6); row < p.M; row += W) {
             if (*wc.abort_flag) break;
             const long long base = row * d;
+            constexpr int NV = 2;
             float ss = 0.f;
-            for (int col = lane * 8; col < d; col += 256) {
-                float h[8];
-                row_h8(p, base + col, h);
+            for (int col0 = lane * 8; col0 < d; col0 += 256 * NV) {
+                float h[NV][8];
+                row_h<NV>(p, base, col0, h);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(h[e], h[e], ss);
+                for (int v = 0; v < NV; ++v)
+                    if (col0 + 256 * v < d)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(h[v][e], h[v][e], ss);
             }
             ss = warp_sum(ss);
             const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
-            for (int col = lane * 8; col < d; col += 256) {
-                float h[8], gm[8];
-                row_h8(p, base + col, h);  // same inputs and order: the same h
-                load8(static_cast<const __nv_bfloat16*>(p.gamma) + col, gm);
-                if (p.h_out != nullptr) __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.h_out) + base + col), pack8(h));
+            for (int col0 = lane * 8; col0 < d; col0 += 256 * NV) {
+                float h[NV][8];
+                row_h<NV>(p, base, col0, h);  // same inputs and order: the same h
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gm[e] = h[e] * inv * gm[e];
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + base + col) = pack8(gm);
+                for (int v = 0; v < NV; ++v) {
+                    const int col = col0 + 256 * v;
+                    if (col < d) {
+                        float gm[8];
+                        load8(static_cast<const __nv_bfloat16*>(p.gamma) + col, gm);
+                        if (p.h_out != nullptr)
+                            __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.h_out) + base + col),
+                                   pack8(h[v]));
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gm[e] = h[v][e] * inv * gm[e];
+                        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + base + col) = pack8(gm);
+                    }
+                }
             }
             // make the row's y visible to the TMA loads of other CTAs
             fence_proxy_async_global();
@@ -313,7 +382,8 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             const bool ok = mbar_wait(&bars->acc_full[acc], acc_phase, wc, kWhereEpilogueAccFull, t);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            // the four epilogue warps leave together (they share barrier 1)
+            if (epilogue_any(!ok)) break;
             tc_fence_after();
             const Tile tl = decode(p, t);
             const int row = tl.m * PBM + row_in_tile;

@@ -32,6 +32,8 @@ enum : int {
     kWhereSelftestBarrier = 7,
     kWherePrologueFull = 8,
     kWherePrologueEmpty = 9,
+    kWhereFusedRows = 10,
+    kWhereFusedGateUp = 11,
 };
 
 // Default limit of every bounded device-side wait (ns). A legitimate wait in
@@ -89,6 +91,36 @@ size_t tc_gemm_smem_bytes();
 // Encodes a 2-D bf16 tensor map (inner = contiguous dim) with 128-byte swizzle.
 bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---------------------------------------------------------------- fused boundary
+// One persistent CTA-pair launch: prologue rows, gate/up + SwiGLU tiles and
+// down tiles with bounded-wait readiness counters between them (bf16).
+struct FusedParams {
+    CUtensorMap mapY;                  // y [M][d], box 64 x 128
+    CUtensorMap mapW1g[kMaxGroups];    // W1g rows F_g [f][d], box 64 x 128
+    CUtensorMap mapW1u[kMaxGroups];    // W1u rows F_g
+    CUtensorMap mapS[kMaxGroups];      // s_g [M][f], box 64 x 128
+    CUtensorMap mapW2[kMaxGroups];     // W2 columns F_g [d][f] (row stride F), box 64 x 128
+    void* s_out[kMaxGroups];           // s_g
+    void* out[kMaxGroups];             // out[g] [M][d]
+    const void* x;                     // [M][d]
+    const void* partials[kMaxGroups];  // [M][d] each
+    const void* gamma;                 // [d]
+    void* h_out;                       // [M][d] or nullptr
+    void* y;                           // [M][d] (workspace)
+    float eps;
+    int M, d, P, f;
+    int mt, nt_gu, nt_dn, nk_gu, nk_dn;   // 256-row tiles
+    int band0, band;                      // m-tiles of the first gate/up band, of the others
+    int tiles_gu, tiles_dn;
+    int* rb_ready;                     // [mt] prologue rows done per 256-row block
+    int* gu_done;                      // [P][mt] gate/up tile halves stored
+    DeviceStatus* status;
+    unsigned long long wait_limit_ns;
+};
+
+int fused_max_pairs(int num_sms);
+cudaError_t launch_boundary_fused(const FusedParams& p, int pairs, cudaStream_t s);
 
 // ---------------------------------------------------------------- fp32 SIMT GEMM
 struct SimtGemmParams {

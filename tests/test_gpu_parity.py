@@ -23,9 +23,12 @@ def _lib():
     torch.cuda.set_device(0)
 
 
-@pytest.fixture(params=["pair", "single"])
+@pytest.fixture(params=["fused", "pair", "single"])
 def gemm_variant(request, monkeypatch):
-    """Runs a test with the CTA-pair (default) and the single-CTA tcgen05 GEMMs."""
+    """Runs a test with each bf16 execution variant: the fused persistent
+    boundary (default), and the three-launch paths on CTA-pair or single-CTA
+    tcgen05 GEMMs (the step-level entry points use the CTA-pair GEMMs unless
+    "single" is selected)."""
     monkeypatch.setenv("SPTP_GEMM_VARIANT", request.param)
     return request.param
 
@@ -150,13 +153,15 @@ def test_boundary_d4096_full_size_sampled_rows(gemm_variant):
     check(*run_boundary(cfg, rows=sample_rows(cfg.M)), "bf16")
 
 
-def test_boundary_qwen2_7b_shape_full_size_sampled_rows():
+def test_boundary_qwen2_7b_shape_full_size_sampled_rows(gemm_variant):
     cfg = synth.QWEN2_7B_SHAPE
     check(*run_boundary(cfg, rows=sample_rows(cfg.M, 16)), "bf16")
 
 
 @pytest.mark.parametrize("M", [4096, 16384, 65536])
-def test_m_sweep_full_size_sampled_rows(M):
+def test_m_sweep_full_size_sampled_rows(M, gemm_variant):
+    if gemm_variant == "single" and M > 4096:
+        pytest.skip("single-CTA variant covered at M=4096")
     cfg = synth.m_sweep(M)
     check(*run_boundary(cfg, rows=sample_rows(cfg.M, 8)), "bf16")
     torch.cuda.empty_cache()
