@@ -39,6 +39,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["boundary", "dtp", "attn", "permute"], default="boundary",
+                    help="boundary: the SP-TP FFN boundary (the default, headline line); the others measure "
+                         "the Delayed-TP stack, the attention-side boundary and the neuron permutation")
     return ap.parse_args()
 
 
@@ -445,10 +448,109 @@ def run_ours(args):
     return 0
 
 
+def timed(fn, steps, warmup, stream):
+    import torch
+    for _ in range(max(3, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_other(args):
+    """Measurement lines for the Delayed-TP stack, the attention-side boundary
+    and the neuron-permutation gather (one GPU, device-resident inputs)."""
+    import torch
+    import sequence_tensor_transformer_gb300 as st
+    from sequence_tensor_transformer_gb300 import synth
+
+    torch.cuda.set_device(0)
+    st.load_library()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    line = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic", "vs_baseline": None}
+    if args.workload == "dtp":
+        cfg = synth.DTP_STACK
+        inp = synth.dtp_inputs(cfg)
+        T = {k: to_dev(v) for k, v in inp.items()}
+        xs0 = T["x_shards"].clone()
+        ws = torch.empty(st.dtp_ffn_stack_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.L, cfg.delta,
+                                                         st.SPTP_BF16), dtype=torch.uint8, device=dev)
+
+        def fn():
+            T["x_shards"].copy_(xs0)
+            st.dtp_ffn_stack_forward(T["x_shards"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.L,
+                                     cfg.delta, 1, cfg.eps, workspace=ws)
+        ms = timed(fn, args.steps, args.warmup, stream)
+        fl = 6.0 * cfg.M * cfg.d * cfg.F * cfg.L
+        value = fl / (ms * 1e-3) / 1e12
+        line.update(metric="Delayed-TP FFN stack forward TFLOP/s", value=value, unit="TFLOP/s", ms_per_step=ms,
+                    tokens_per_s=cfg.M / (ms * 1e-3), config={"workload": cfg.name},
+                    roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                              "frac": value / pk["bf16_sustained"], "note": "whole stack incl. the stream copy-in "
+                              "(4 prologues + 8 GEMM launches + flush per step)"})
+    elif args.workload == "attn":
+        cfg = synth.ATTN_QWEN2_7B_SHAPE
+        inp = synth.attn_inputs(cfg)
+        T = {k: to_dev(v) for k, v in inp.items()}
+        qkv = torch.empty((cfg.P, cfg.M, cfg.N // cfg.P), dtype=torch.bfloat16, device=dev)
+        h = torch.empty_like(T["x"])
+        out = torch.empty((cfg.P, cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(st.sptp_attn_qkv_workspace_size(cfg.M, cfg.d, cfg.N, cfg.P, cfg.chunks, st.SPTP_BF16),
+                         dtype=torch.uint8, device=dev)
+        hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
+        ms_q = timed(lambda: st.sptp_attn_qkv_forward(T["x"], T["partials"], T["gamma"], T["Wqkv"], cfg.P,
+                                                      cfg.chunks, cfg.eps, qkv_out=qkv, resid_out=h, workspace=ws),
+                     args.steps, args.warmup, stream)
+        ms_o = timed(lambda: st.sptp_down_proj(T["attn"], T["Wo"], cfg.P, out=out, workspace=hdr), args.steps,
+                     args.warmup, stream)
+        fq, fo = 2.0 * cfg.M * cfg.d * cfg.N, 2.0 * cfg.M * cfg.Ho * cfg.d
+        value = (fq + fo) / ((ms_q + ms_o) * 1e-3) / 1e12
+        line.update(metric="attention-side boundary (QKV boundary + row-parallel out-projection) TFLOP/s",
+                    value=value, unit="TFLOP/s", ms_per_step=ms_q + ms_o, config={"workload": cfg.name},
+                    kernels={"qkv_boundary": {"ms": ms_q, "achieved": fq / (ms_q * 1e-3) / 1e12},
+                             "out_projection": {"ms": ms_o, "achieved": fo / (ms_o * 1e-3) / 1e12}},
+                    roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                              "frac": value / pk["bf16_sustained"]})
+    else:
+        cfg = synth.DTP_STACK
+        inp = synth.dtp_inputs(cfg)
+        T = {k: to_dev(inp[k]) for k in ("W1g", "W1u", "W2")}
+        rng = np.random.default_rng(0)
+        perm = torch.from_numpy(np.stack([rng.permutation(cfg.F) for _ in range(cfg.L)]).astype(np.int32)).to(dev)
+        hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
+        outs = [torch.empty_like(T["W1g"]), torch.empty_like(T["W1u"]), torch.empty_like(T["W2"])]
+
+        def fn():
+            st.lib().sptp_permute_ffn_neurons(
+                T["W1g"].data_ptr(), T["W1u"].data_ptr(), T["W2"].data_ptr(), perm.data_ptr(), cfg.L, cfg.d,
+                cfg.F, st.SPTP_BF16, outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), hdr.data_ptr(),
+                hdr.numel(), stream.cuda_stream)
+        ms = timed(fn, args.steps, args.warmup, stream)
+        by = 2.0 * 3 * cfg.L * cfg.F * cfg.d * 2
+        gbs = by / (ms * 1e-3) / 1e9
+        line.update(metric="neuron-permutation shard map (W1g/W1u rows + W2 columns) GB/s", value=gbs, unit="GB/s",
+                    ms_per_step=ms, config={"workload": cfg.name + "_permute"},
+                    roofline={"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
+                              "frac": gbs / pk["hbm"], "algorithmic_bytes": by})
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "boundary":
+        return run_other(args)
     return run_ours(args)
 
 

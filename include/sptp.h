@@ -151,17 +151,66 @@ int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u,
 /*
  * sptp_down_proj -- row-parallel down GEMM per shard ([A] "Potential
  * Solution"): out[p] = s[p] W2[:, F_p]^T with s [P][M][F/P], out [P][M][d].
- * workspace: at least SPTP_WS_HEADER_BYTES.
+ * Also the row-parallel output projection of an attention sub-layer (s = the
+ * per-shard attention output, W2 = Wo [d][F]).  workspace: at least
+ * SPTP_WS_HEADER_BYTES.
  */
 int sptp_down_proj(const void* s, const void* W2, int M, int d, int F, int P, int dtype,
                    void* out, void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/* Workspace bytes needed by sptp_attn_qkv_forward (0 on bad args).
+ * Layout: header | y [M][d]. */
+size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, int dtype);
+
+/*
+ * sptp_attn_qkv_forward -- the sub-layer boundary in front of an attention
+ * sub-layer ([A] "Potential Solution": 4 boundaries per block, between the
+ * attention and FFN sub-layers both ways).  Steps 1-3 as in
+ * sptp_ffn_forward (partial sum, residual add, RMSNorm), the (identity)
+ * chunked gather, then each shard's column-parallel QKV projection:
+ *     qkv_out[p] = y Wqkv[p*N/P .. (p+1)*N/P)^T
+ *   Wqkv      [N][d]: shard p owns rows [p*N/P, (p+1)*N/P) (its heads' q, k
+ *             and v rows, arranged by the caller); N % P == 0, (N/P) % 8 == 0
+ *   qkv_out   [P][M][N/P]; resid_out, chunks, eps, dtype, workspace and the
+ *   shape rules as in sptp_ffn_forward.
+ * The row-parallel output projection after attention, which yields the next
+ * P partials, is sptp_down_proj with F = the attention width (attn [P][M][F/P],
+ * Wo [d][F]).
+ */
+int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma, const void* Wqkv,
+                          int M, int d, int N, int P, int chunks, float eps, int dtype,
+                          void* qkv_out, void* resid_out,
+                          void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/*
+ * sptp_permute_ffn_neurons -- executes a neuron-permutation shard map for
+ * Delayed TP ([B], Abstract: the dense model is permuted before it is
+ * sharded; with delayed partials, which neurons share a device changes the
+ * model).  For every module l and new neuron i, new neuron i is old neuron
+ * perm[l][i]:
+ *     W1g_out[l][i][:] = W1g[l][perm[l][i]][:],  W1u_out likewise,
+ *     W2_out[l][:][i]  = W2[l][:][perm[l][i]].
+ * Contiguous sharding of the outputs (dtp_ffn_stack_forward) then gives
+ * shard p the old neurons perm[l][F_p].
+ *   W1g, W1u [L][F][d];  W2 [L][d][F];  perm: DEVICE int32 [L][F], meant to
+ *   be a permutation of 0..F-1 per module.  An entry outside [0, F) is
+ *   recorded as SPTP_ERR_SHAPE in the workspace status words (see
+ *   sptp_read_device_status) and its outputs are zero-filled.
+ *   Outputs must not overlap the inputs or each other.  F*sizeof(dtype) <=
+ *   200 KiB.  workspace: at least SPTP_WS_HEADER_BYTES.
+ */
+int sptp_permute_ffn_neurons(const void* W1g, const void* W1u, const void* W2, const int* perm,
+                             int L, int d, int F, int dtype,
+                             void* W1g_out, void* W1u_out, void* W2_out,
+                             void* workspace, size_t ws_bytes, void* cuda_stream);
 
 /*
  * sptp_read_device_status -- synchronises `cuda_stream` and returns the
  * status the kernels recorded in the workspace header since the last call
  * that reset it (every entry point above resets it when it starts):
- * SPTP_OK, or SPTP_ERR_TIMEOUT if a bounded device-side wait ran out (the
- * kernels then stop early and their outputs are undefined).  No counterpart
+ * SPTP_OK; SPTP_ERR_TIMEOUT if a bounded device-side wait ran out (the
+ * kernels then stop early and their outputs are undefined); or
+ * SPTP_ERR_SHAPE if sptp_permute_ffn_neurons met an index outside [0, F).  No counterpart
  * on the pages: this is the library's own failure detection.
  */
 int sptp_read_device_status(const void* workspace, void* cuda_stream);

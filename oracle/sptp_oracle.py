@@ -172,6 +172,70 @@ def dtp_ffn_stack_forward(x_shards, gamma, W1g, W1u, W2, P: int, L: int, delta: 
     return x
 
 
+def attn_qkv_boundary(x, partials, gamma, Wqkv, P: int, chunks: int, eps: float):
+    """The boundary in front of an attention sub-layer (page 1, "Potential
+    Solution": there are 4 boundaries per block, between attention and FFN
+    sub-layers both ways).  The same reduce-scatter arithmetic, residual add
+    and RMSNorm per chunk, then the (identity) all-gather and each shard's
+    column-parallel QKV projection: shard p holds rows
+    [p N/P, (p+1) N/P) of Wqkv [N][d] (its heads' q, k and v rows).
+
+    Returns (qkv [P, M, N/P], h [M, d])."""
+    M, d = x.shape
+    N = Wqkv.shape[0]
+    if partials.shape[0] != P or N % P != 0 or chunks < 1 or M % chunks != 0:
+        raise ValueError("bad shape")
+    n = N // P
+    qkv = np.zeros((P, M, n))
+    h_out = np.zeros((M, d))
+    m = M // chunks
+    for c in range(chunks):
+        rows = slice(c * m, (c + 1) * m)
+        h = x[rows] + reduce_partials(partials[:, rows, :])
+        y = rms_norm(h, gamma, eps)
+        h_out[rows] = h
+        for p in range(P):
+            qkv[p, rows] = y @ Wqkv[p * n:(p + 1) * n].T
+    return qkv, h_out
+
+
+def rowparallel_projection(a, W, P: int):
+    """Row-parallel projection after a sub-layer (page 1, "Potential
+    Solution": the sub-layer ends with a reduce-scatter of these partials):
+    shard p multiplies its activations a[p] [M][K/P] by its columns
+    [p K/P, (p+1) K/P) of W [d][K] and yields a full-width partial."""
+    K = W.shape[1]
+    k = K // P
+    return np.stack([a[p] @ W[:, p * k:(p + 1) * k].T for p in range(P)])
+
+
+def permute_ffn_neurons(W1g: np.ndarray, W1u: np.ndarray, W2: np.ndarray, perm) -> tuple:
+    """One FFN with its neurons renumbered before sharding (page 2, Abstract:
+    the dense model is permuted before it is sharded, so the contiguous
+    shard p then holds the old neurons perm[F_p]).  New neuron i is old
+    neuron perm[i]: rows of W1g/W1u and columns of W2 move together."""
+    perm = np.asarray(perm)
+    if sorted(perm.tolist()) != list(range(W1g.shape[0])):
+        raise ValueError("not a permutation")
+    return W1g[perm], W1u[perm], W2[:, perm]
+
+
+def dtp_ffn_stack_forward_permuted(x_shards, gamma, W1g, W1u, W2, perms, P: int, L: int, delta: int,
+                                   flush: bool, eps: float, rows=None):
+    """Delayed-TP stack under a neuron-permutation shard map per module
+    (page 2, Abstract: with delayed partials the sharding is a modelling
+    decision).  perms[l] renumbers module l's neurons before contiguous
+    sharding; see permute_ffn_neurons."""
+    g1, u1, w2 = [], [], []
+    for l in range(L):
+        a, b, c = permute_ffn_neurons(W1g[l], W1u[l], W2[l], perms[l])
+        g1.append(a)
+        u1.append(b)
+        w2.append(c)
+    return dtp_ffn_stack_forward(x_shards, gamma, np.stack(g1), np.stack(u1), np.stack(w2), P, L, delta, flush,
+                                 eps, rows=rows)
+
+
 def rel_max_error(got: np.ndarray, ref: np.ndarray) -> float:
     """max_i |got_i - ref_i| / max_i |ref_i| (0 when both are all zero)."""
     got = np.asarray(got, dtype=np.float64)

@@ -17,7 +17,8 @@ __all__ = [
     "sptp_ffn_workspace_size", "sptp_ffn_forward", "dtp_ffn_stack_workspace_size",
     "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
     "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "EXPORTED_SYMBOLS",
-    "sptp_ffn_forward_noalloc", "SPTP_NOALLOC_SCRATCH_BYTES",
+    "sptp_ffn_forward_noalloc", "SPTP_NOALLOC_SCRATCH_BYTES", "sptp_permute_ffn_neurons",
+    "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward",
 ]
 
 SPTP_BF16 = 0
@@ -30,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "sptp_ffn_workspace_size", "sptp_ffn_forward", "dtp_ffn_stack_workspace_size",
     "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
     "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "sptp_ffn_forward_noalloc",
+    "sptp_permute_ffn_neurons", "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward",
 )
 
 _lib = None
@@ -47,6 +49,9 @@ _SIGS = {
     "sptp_wait_selftest": (_I, [_P, _Z, _U64, _I, _P]),
     "sptp_status_string": (ctypes.c_char_p, [_I]),
     "sptp_ffn_forward_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
+    "sptp_permute_ffn_neurons": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "sptp_attn_qkv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
+    "sptp_attn_qkv_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _Z, _P]),
 }
 
 
@@ -208,6 +213,45 @@ def sptp_ffn_forward_noalloc(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, o
         _dtype_code(x), _ptr(out), _ptr(resid_out), _stream(stream))
     _check("sptp_ffn_forward_noalloc", code)
     return out, resid_out
+
+
+def sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dtype=SPTP_BF16) -> int:
+    return int(lib().sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dtype))
+
+
+def sptp_attn_qkv_forward(x, partials, gamma, Wqkv, P, chunks, eps, qkv_out=None, resid_out=None,
+                          workspace=None, stream=None, write_resid=True):
+    """Boundary in front of attention: returns (qkv [P,M,N/P], resid_out)."""
+    M, d = x.shape
+    N = Wqkv.shape[0]
+    dt = _dtype_code(x)
+    if qkv_out is None:
+        qkv_out = torch.empty((P, M, N // P), dtype=x.dtype, device=x.device)
+    if resid_out is None and write_resid:
+        resid_out = torch.empty_like(x)
+    if workspace is None:
+        workspace = _workspace(sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dt), x.device)
+    code = lib().sptp_attn_qkv_forward(_ptr(x), _ptr(partials), _ptr(gamma), _ptr(Wqkv), M, d, N, P, chunks,
+                                       float(eps), dt, _ptr(qkv_out), _ptr(resid_out), _ptr(workspace),
+                                       workspace.numel(), _stream(stream))
+    _check("sptp_attn_qkv_forward", code)
+    return qkv_out, resid_out
+
+
+def sptp_permute_ffn_neurons(W1g, W1u, W2, perm, workspace=None, stream=None):
+    """Renumbers every module's neurons (W1g/W1u [L,F,d] rows, W2 [L,d,F]
+    columns) by perm [L,F] (int32, device); returns the permuted copies."""
+    L, F, d = W1g.shape
+    outs = [torch.empty_like(W1g), torch.empty_like(W1u), torch.empty_like(W2)]
+    if workspace is None:
+        workspace = _workspace(SPTP_WS_HEADER_BYTES, W1g.device)
+    if perm.dtype != torch.int32:
+        raise TypeError("perm must be int32")
+    code = lib().sptp_permute_ffn_neurons(_ptr(W1g), _ptr(W1u), _ptr(W2), _ptr(perm), L, d, F, _dtype_code(W1g),
+                                          _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(workspace),
+                                          workspace.numel(), _stream(stream))
+    _check("sptp_permute_ffn_neurons", code)
+    return tuple(outs)
 
 
 def sptp_read_device_status(workspace, stream=None) -> int:

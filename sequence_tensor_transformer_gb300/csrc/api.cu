@@ -215,6 +215,59 @@ int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype
     return cuda_status(launch_simt_gemm(p, Epi::kStore, s));
 }
 
+// Column-parallel projection for P groups with a plain bf16/fp32 store:
+// out_g [M][N/P] = A W[g*N/P .. (g+1)*N/P)^T, W [N][K] row-major.
+int colpar_store(const void* A, const void* W, int M, int K, int N, int P, int dtype, void* out, DeviceStatus* st,
+                 int band, const DevInfo& di, cudaStream_t s) {
+    const int n = N / P;
+    const size_t es = esize(dtype);
+    if (M == 0) return SPTP_OK;
+    if (dtype == SPTP_BF16) {
+        const bool pair = use_pair_gemm();
+        const int bm = pair ? 2 * kBM : kBM;
+        const uint32_t bbox = pair ? kBNStore / 2 : kBNStore;
+        TcGemmParams p;
+        std::memset(&p, 0, sizeof(p));
+        for (int g = 0; g < P; ++g) {
+            if (!encode_map_bf16(&p.mapA[g], A, K, M, static_cast<uint64_t>(K) * es, kBK, kBM) ||
+                !encode_map_bf16(&p.mapB0[g], cptr(W, static_cast<size_t>(g) * n * K * es), K, n,
+                                 static_cast<uint64_t>(K) * es, kBK, bbox))
+                return SPTP_ERR_CUDA;
+            p.out[g] = mptr(out, static_cast<size_t>(g) * M * n * es);
+        }
+        p.ldo = n;
+        p.M = M;
+        p.N = n;
+        p.K = K;
+        p.G = P;
+        p.mt = (M + bm - 1) / bm;
+        p.nt = (n + kBNStore - 1) / kBNStore;
+        p.nk = (K + kBK - 1) / kBK;
+        if (pair) band = (band + 1) / 2;
+        p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
+        p.status = st;
+        p.wait_limit_ns = kWaitLimitNs;
+        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kStore, di.sms, s)
+                                : launch_tc_gemm(p, Epi::kStore, di.sms, s));
+    }
+    SimtGemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int g = 0; g < P; ++g) {
+        p.A[g] = static_cast<const float*>(A);
+        p.B0[g] = static_cast<const float*>(W) + static_cast<size_t>(g) * n * K;
+        p.B1[g] = nullptr;
+        p.C[g] = static_cast<float*>(out) + static_cast<size_t>(g) * M * n;
+    }
+    p.lda = K;
+    p.ldb = K;
+    p.ldc = n;
+    p.M = M;
+    p.N = n;
+    p.K = K;
+    p.G = P;
+    return cuda_status(launch_simt_gemm(p, Epi::kStore, s));
+}
+
 // Readiness counters of the fused boundary: per 256-row block, prologue rows
 // done; per (shard, 256-row block), gate/up tile halves stored.
 size_t fused_counter_bytes(int M, int P) {
@@ -600,6 +653,96 @@ int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P,
     void* outs[kMaxGroups];
     for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * M * d * es);
     return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), band_for_chunks(M, 1), di, s);
+}
+
+size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, int dtype) {
+    if (check_common(M, d, N, P, dtype) != SPTP_OK || chunks < 1) return 0;
+    return SPTP_WS_HEADER_BYTES + align_up(static_cast<size_t>(M) * d * esize(dtype));
+}
+
+int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma, const void* Wqkv, int M, int d,
+                          int N, int P, int chunks, float eps, int dtype, void* qkv_out, void* resid_out,
+                          void* workspace, size_t ws_bytes, void* cuda_stream) {
+    if (!gamma || !Wqkv || !workspace || (M != 0 && (!x || !partials || !qkv_out))) return SPTP_ERR_NULL;
+    int rc = check_common(M, d, N, P, dtype);
+    if (rc != SPTP_OK) return rc;
+    if (chunks < 1 || chunks % P != 0 || (M > 0 && M % chunks != 0)) return SPTP_ERR_SHAPE;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
+    const void* ptrs[] = {x, partials, gamma, Wqkv, qkv_out, resid_out, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return SPTP_ERR_SHAPE;
+    const size_t need = sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dtype);
+    if (ws_bytes < need) return SPTP_ERR_WORKSPACE;
+    const size_t es = esize(dtype);
+    const size_t act = static_cast<size_t>(M) * d * es;
+    const size_t qb = static_cast<size_t>(M) * N * es, wb = static_cast<size_t>(N) * d * es;
+    const void* ins[] = {x, partials, gamma, Wqkv, workspace, resid_out};
+    const size_t insz[] = {act, act * P, d * es, wb, need, resid_out ? act : 0};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(qkv_out, qb, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    const void* wins[] = {x, partials, gamma, Wqkv};
+    const size_t wsz[] = {act, act * P, d * es, wb};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(workspace, need, wins[i], wsz[i])) return SPTP_ERR_ALIAS;
+    if (resid_out && resid_out != x) {
+        const void* rins[] = {x, partials, gamma, Wqkv, workspace};
+        const size_t rsz[] = {act, act * P, d * es, wb, need};
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(resid_out, act, rins[i], rsz[i])) return SPTP_ERR_ALIAS;
+    }
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    void* y = mptr(workspace, SPTP_WS_HEADER_BYTES);
+    PrologueParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.G = 1;
+    pp.M = M;
+    pp.d = d;
+    pp.eps = eps;
+    pp.gamma = gamma;
+    pp.grp[0] = PrologueGroup{x, resid_out, y, 0, P};
+    for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
+    pp.status = ws_status(workspace);
+    pp.wait_limit_ns = kWaitLimitNs;
+    if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
+    return colpar_store(y, Wqkv, M, d, N, P, dtype, qkv_out, ws_status(workspace), band_for_chunks(M, chunks), di,
+                        s);
+}
+
+int sptp_permute_ffn_neurons(const void* W1g, const void* W1u, const void* W2, const int* perm, int L, int d,
+                             int F, int dtype, void* W1g_out, void* W1u_out, void* W2_out, void* workspace,
+                             size_t ws_bytes, void* cuda_stream) {
+    if (!W1g || !W1u || !W2 || !perm || !W1g_out || !W1u_out || !W2_out || !workspace) return SPTP_ERR_NULL;
+    int rc = check_common(8, d, F, 1, dtype);
+    if (rc != SPTP_OK) return rc;
+    if (L < 1) return SPTP_ERR_SHAPE;
+    const size_t es = esize(dtype);
+    if (static_cast<size_t>(F) * es > 200u * 1024u) return SPTP_ERR_SHAPE;  // one W2 row in shared memory
+    if (ws_bytes < SPTP_WS_HEADER_BYTES) return SPTP_ERR_WORKSPACE;
+    const void* ptrs[] = {W1g, W1u, W2, W1g_out, W1u_out, W2_out, workspace};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return SPTP_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(perm) & 3u) != 0) return SPTP_ERR_SHAPE;
+    const size_t wb = static_cast<size_t>(L) * F * d * es;
+    const void* outs[] = {W1g_out, W1u_out, W2_out};
+    const void* ins[] = {W1g, W1u, W2, perm, workspace};
+    const size_t insz[] = {wb, wb, wb, static_cast<size_t>(L) * F * sizeof(int), SPTP_WS_HEADER_BYTES};
+    for (const void* o : outs) {
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(o, wb, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+        for (const void* o2 : outs)
+            if (o2 != o && overlaps(o, wb, o2, wb)) return SPTP_ERR_ALIAS;
+    }
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    return cuda_status(launch_permute_ffn(W1g, W1u, W2, perm, L, d, F, dtype == SPTP_BF16, W1g_out, W1u_out, W2_out,
+                                          ws_status(workspace), di.sms, s));
 }
 
 int sptp_read_device_status(const void* workspace, void* cuda_stream) {

@@ -34,6 +34,7 @@ enum : int {
     kWherePrologueEmpty = 9,
     kWhereFusedRows = 10,
     kWhereFusedGateUp = 11,
+    kWherePermIndex = 12,
 };
 
 // Default limit of every bounded device-side wait (ns). A legitimate wait in
@@ -133,6 +134,11 @@ struct SimtGemmParams {
 };
 
 cudaError_t launch_simt_gemm(const SimtGemmParams& p, Epi epi, cudaStream_t s);
+
+// ---------------------------------------------------------------- neuron permutation
+cudaError_t launch_permute_ffn(const void* W1g, const void* W1u, const void* W2, const int* perm, int L, int d,
+                               int F, bool bf16, void* W1g_out, void* W1u_out, void* W2_out, DeviceStatus* st,
+                               int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- self-test
 cudaError_t launch_wait_selftest(DeviceStatus* st, unsigned long long limit_ns, cudaStream_t s);

@@ -81,6 +81,28 @@ M_SWEEP = tuple(m_sweep(M) for M in (4096, 8192, 16384, 32768, 65536))
 DTP_STACK = DTPConfig("dtp_bf16_L4_M4096_d1024_F3072_P2_delta1", 4096, 1024, 3072, 2, 4, 1, "bf16")
 
 
+@dataclasses.dataclass(frozen=True)
+class AttnConfig:
+    """The boundary in front of an attention sub-layer and the row-parallel
+    projection after it: N = q + k + v projection rows, Ho = attention width."""
+
+    name: str
+    M: int
+    d: int
+    N: int
+    Ho: int
+    P: int
+    chunks: int
+    dtype: str
+    eps: float = 1e-6
+    seed: int = 0
+
+
+# Qwen2-7B-shaped attention: 28 query heads and 4 key/value heads of 128
+ATTN_QWEN2_7B_SHAPE = AttnConfig("attn_bf16_M16384_d3584_N4608_Ho3584_P4_C16", 16384, 3584,
+                                 28 * 128 + 2 * 4 * 128, 28 * 128, 4, 16, "bf16")
+
+
 # ---------------------------------------------------------------- drawing
 
 def _block(seed: int, tid: int, b: int, n: int) -> np.ndarray:
@@ -180,3 +202,19 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 def to_f64(arr: np.ndarray, dtype: str) -> np.ndarray:
     """Widen a storage-format array to float64 (exact)."""
     return bf16_bits_to_f64(arr) if dtype == "bf16" else arr.astype(np.float64)
+
+
+def attn_inputs(cfg: AttnConfig) -> dict:
+    """Inputs of the attention-side boundary, in storage format: x[M][d],
+    partials[P][M][d], gamma[d], Wqkv[N][d] ~ N(0, 1/d); and of the
+    row-parallel output projection: attn[P][M][Ho/P] ~ N(0, 1), Wo[d][Ho] ~
+    N(0, 1/Ho).  Tensor ids 20.. keep the draws apart from the FFN's."""
+    M, d, N, Ho, P, s, dt = cfg.M, cfg.d, cfg.N, cfg.Ho, cfg.P, cfg.seed, cfg.dtype
+    return {
+        "x": draw((M, d), 1.0, 0.0, dt, s, 20),
+        "partials": draw((P, M, d), 1.0, 0.0, dt, s, 21),
+        "gamma": draw((d,), 0.1, 1.0, dt, s, 22),
+        "Wqkv": draw((N, d), d ** -0.5, 0.0, dt, s, 23),
+        "attn": draw((P, M, Ho // P), 1.0, 0.0, dt, s, 24),
+        "Wo": draw((d, Ho), Ho ** -0.5, 0.0, dt, s, 25),
+    }

@@ -319,3 +319,109 @@ def test_synthetic_inputs_are_seeded_and_shaped():
     big = synth.draw((3, synth.BLOCK // 2 + 5), 1.0, 0.0, "bf16", 0, 7)
     again = synth.draw((3, synth.BLOCK // 2 + 5), 1.0, 0.0, "bf16", 0, 7)
     assert np.array_equal(big, again)
+
+
+# ------------------------------------------------------------ neuron-permutation shard maps
+
+def _perms(L, F, rng, kind):
+    out = []
+    for _ in range(L):
+        if kind == "identity":
+            out.append(np.arange(F))
+        elif kind == "within":
+            # reorder neurons inside each of the 2 contiguous shards only
+            f = F // 2
+            out.append(np.concatenate([rng.permutation(f), f + rng.permutation(f)]))
+        else:
+            out.append(rng.permutation(F))
+    return out
+
+
+def test_permutation_of_a_single_ffn_moves_rows_and_columns_together():
+    rng = np.random.default_rng(4)
+    W1g, W1u, W2 = rng.standard_normal((8, 3)), rng.standard_normal((8, 3)), rng.standard_normal((3, 8))
+    perm = rng.permutation(8)
+    a, b, c = oracle.permute_ffn_neurons(W1g, W1u, W2, perm)
+    for i in range(8):
+        assert np.array_equal(a[i], W1g[perm[i]]) and np.array_equal(b[i], W1u[perm[i]])
+        assert np.array_equal(c[:, i], W2[:, perm[i]])
+    with pytest.raises(ValueError):
+        oracle.permute_ffn_neurons(W1g, W1u, W2, [0] * 8)
+
+
+@pytest.mark.parametrize("kind", ["identity", "random"])
+def test_tp_is_invariant_to_any_neuron_permutation(kind):
+    """delta = 0 sums every neuron's contribution, so renumbering neurons
+    before sharding cannot change the result (the symmetry DTP breaks)."""
+    M, d, F, P, L = 6, 16, 32, 2, 3
+    x0, gamma, W1g, W1u, W2 = dtp_case(M, d, F, P, L)
+    xs = np.stack([x0] * P)
+    ref = dtp_ffn_stack_forward(xs, gamma, W1g, W1u, W2, P, L, 0, 1, 1e-6)
+    got = oracle.dtp_ffn_stack_forward_permuted(xs, gamma, W1g, W1u, W2, _perms(L, F, np.random.default_rng(1),
+                                                kind), P, L, 0, 1, 1e-6)
+    assert rel_max_error(got, ref) < 1e-12
+
+
+@pytest.mark.parametrize("delta", [1, 2])
+def test_dtp_is_invariant_to_reordering_within_shards(delta):
+    M, d, F, P, L = 6, 16, 32, 2, 3
+    x0, gamma, W1g, W1u, W2 = dtp_case(M, d, F, P, L)
+    xs = np.stack([x0] * P)
+    ref = dtp_ffn_stack_forward(xs, gamma, W1g, W1u, W2, P, L, delta, 0, 1e-6)
+    got = oracle.dtp_ffn_stack_forward_permuted(xs, gamma, W1g, W1u, W2, _perms(L, F, np.random.default_rng(2),
+                                                "within"), P, L, delta, 0, 1e-6)
+    assert rel_max_error(got, ref) < 1e-12
+
+
+def test_dtp_depends_on_which_neurons_share_a_shard():
+    """With delayed partials a cross-shard renumbering changes the streams:
+    the sharding is a modelling decision."""
+    M, d, F, P, L = 6, 16, 32, 2, 3
+    x0, gamma, W1g, W1u, W2 = dtp_case(M, d, F, P, L)
+    xs = np.stack([x0] * P)
+    ref = dtp_ffn_stack_forward(xs, gamma, W1g, W1u, W2, P, L, 1, 0, 1e-6)
+    got = oracle.dtp_ffn_stack_forward_permuted(xs, gamma, W1g, W1u, W2, _perms(L, F, np.random.default_rng(3),
+                                                "random"), P, L, 1, 0, 1e-6)
+    assert rel_max_error(got, ref) > 1e-3
+
+
+# ------------------------------------------------------------ attention-side boundary
+
+def test_attn_qkv_boundary_unsharded_matches_torch_functional():
+    M, d, N = 12, 32, 48
+    rng = np.random.default_rng(21)
+    x, parts = rng.standard_normal((M, d)), rng.standard_normal((2, M, d))
+    gamma = 1 + 0.1 * rng.standard_normal(d)
+    W = rng.standard_normal((N, d)) / math.sqrt(d)
+    qkv2, h2 = oracle.attn_qkv_boundary(x, parts, gamma, W, 2, 2, 1e-6)
+    T = torch.from_numpy
+    y = Fn.rms_norm(T(x) + T(parts).sum(0), (d,), T(gamma), 1e-6)
+    ref = Fn.linear(y, T(W)).numpy()
+    assert rel_max_error(np.concatenate([qkv2[0], qkv2[1]], axis=1), ref) < 1e-13
+    assert rel_max_error(h2, (T(x) + T(parts).sum(0)).numpy()) < 1e-15
+
+
+def test_rowparallel_projection_partials_sum_to_the_full_linear():
+    rng = np.random.default_rng(22)
+    P, M, K, d = 4, 10, 64, 24
+    a = rng.standard_normal((P, M, K // P))
+    W = rng.standard_normal((d, K))
+    out = oracle.rowparallel_projection(a, W, P)
+    full = Fn.linear(torch.from_numpy(np.concatenate(list(a), axis=1)), torch.from_numpy(W)).numpy()
+    assert rel_max_error(out.sum(0), full) < 1e-13
+    W0 = W.copy()
+    W0[:, K // P:2 * K // P] = 0
+    assert np.all(oracle.rowparallel_projection(a, W0, P)[1] == 0)
+
+
+def test_attn_qkv_boundary_chunking_and_zero_weights():
+    rng = np.random.default_rng(23)
+    M, d, N, P = 16, 24, 32, 2
+    x, parts = rng.standard_normal((M, d)), rng.standard_normal((P, M, d))
+    gamma = 1 + 0.1 * rng.standard_normal(d)
+    W = rng.standard_normal((N, d))
+    a, ha = oracle.attn_qkv_boundary(x, parts, gamma, W, P, P, 1e-6)
+    b, hb = oracle.attn_qkv_boundary(x, parts, gamma, W, P, 8, 1e-6)
+    assert rel_max_error(a, b) < 1e-14 and rel_max_error(ha, hb) == 0.0
+    z, _ = oracle.attn_qkv_boundary(x, parts, gamma, np.zeros_like(W), P, P, 1e-6)
+    assert np.all(z == 0)
