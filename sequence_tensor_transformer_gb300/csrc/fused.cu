@@ -94,7 +94,8 @@ __device__ __forceinline__ Tile decode(const FusedParams& p, int t) {
     return r;
 }
 
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
+// silu with the fast divide (<= 2 ulp in fp32, below the bf16 output rounding)
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

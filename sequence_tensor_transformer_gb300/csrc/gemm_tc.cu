@@ -57,7 +57,10 @@ __device__ __forceinline__ void decode_tile(const TcGemmParams& p, int t, int& g
     n = gn - g * p.nt;
 }
 
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
+// silu(a) = a / (1 + e^-a) with the fast divide (<= 2 ulp in fp32, far below
+// the bf16 rounding of the output); for a < -87 the divisor overflows and the
+// result is 0, the correctly rounded bf16 value there.
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -280,6 +283,8 @@ constexpr int B_BYTES = 128 * BK * 2;        // 16 KiB (half of the B tile)
 constexpr int PSTAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + BAR_BYTES;
 constexpr uint32_t PIDESC = idesc_bf16_f32(PBM, PBN);
+constexpr int PEPI_WARPS = 8;                   // two per TMEM lane quarter
+constexpr int PTHREADS = 32 * (2 + PEPI_WARPS);
 
 struct Bars {
     uint64_t full[PSTAGES];
@@ -293,7 +298,7 @@ struct Bars {
 static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block too large");
 
 template <Epi EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
+__global__ void __launch_bounds__(PTHREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&bars->acc_full[a], 1);
-            mbar_init(&bars->acc_empty[a], 2 * 4 * 32);
+            mbar_init(&bars->acc_empty[a], 2 * PEPI_WARPS * 32);
         }
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
@@ -428,8 +433,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         mbar_wait(&bars->drain, 0, drain, kWhereDrain, -1);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue (both CTAs)
+        // warp w reads TMEM lanes [32*(w%4), +32); warps 2..5 take the first
+        // half of the tile's columns, warps 6..9 the second half
         const uint32_t acc_empty0 = mapa_shared(smem_u32(&bars->acc_empty[0]), 0);
         const int quarter = warp & 3;
+        const int half = (warp - 2) / 4;
         const int row_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
         int local = 0;
         for (int t = pair_id; t < total; t += npairs, ++local) {
@@ -447,7 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[g]) + static_cast<long long>(row) * p.ldo;
             if (EPI == Epi::kSwiGLU) {
 #pragma unroll 1
-                for (int c = 0; c < PBN / 2; c += 32) {
+                for (int c = half * (PBN / 4); c < (half + 1) * (PBN / 4); c += 32) {
                     uint32_t gv[32], uv[32];
                     tmem_ld_32cols(taddr + c, gv);
                     tmem_ld_32cols(taddr + PBN / 2 + c, uv);
@@ -470,7 +478,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                 }
             } else {
 #pragma unroll 1
-                for (int c = 0; c < PBN; c += 32) {
+                for (int c = half * (PBN / 2); c < (half + 1) * (PBN / 2); c += 32) {
                     uint32_t v32[32];
                     tmem_ld_32cols(taddr + c, v32);
                     tmem_ld_wait();
@@ -566,7 +574,7 @@ cudaError_t launch_pair_typed(const TcGemmParams& p, int num_sms, cudaStream_t s
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(pair::PTHREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::PSMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
