@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/sptp.h"
+#include "sptp.h"
 #include "sptp_internal.h"
 
 using namespace sptp;
@@ -268,6 +268,29 @@ int colpar_store(const void* A, const void* W, int M, int K, int N, int P, int d
     return cuda_status(launch_simt_gemm(p, Epi::kStore, s));
 }
 
+// Readiness counters of the fused Delayed-TP stack: per module, rows normed
+// and down halves stored per 256-row block; gate/up halves per (shard, block).
+size_t dtp_counter_bytes(int M, int P, int L) {
+    const size_t mt = (static_cast<size_t>(M) + 255) / 256;
+    return static_cast<size_t>(L) * mt * (2 + static_cast<size_t>(P)) * sizeof(int);
+}
+
+// Delayed-TP execution: one fused persistent launch for the whole stack
+// (bf16; the default) or, with SPTP_DTP_VARIANT=layers, a prologue and two
+// GEMM launches per module.
+bool dtp_fused_selected() {
+    const char* v = std::getenv("SPTP_DTP_VARIANT");
+    return !(v != nullptr && std::strcmp(v, "layers") == 0);
+}
+
+// With SPTP_STRICT_VARIANT=1 a selected fused launch that cannot run is an
+// error (SPTP_ERR_CUDA) instead of a fall-back to the multi-launch path; the
+// tests use it to make sure the variant they name is the one that ran.
+bool strict_variant() {
+    const char* v = std::getenv("SPTP_STRICT_VARIANT");
+    return v != nullptr && std::strcmp(v, "1") == 0;
+}
+
 // Readiness counters of the fused boundary: per 256-row block, prologue rows
 // done; per (shard, 256-row block), gate/up tile halves stored.
 size_t fused_counter_bytes(int M, int P) {
@@ -373,6 +396,97 @@ int fused_forward(const void* x, const void* partials, const void* gamma, const 
     return SPTP_ERR_CUDA;
 }
 
+// The whole bf16 Delayed-TP stack as one persistent launch (fused_dtp.cu).
+// Returns SPTP_ERR_UNSUPPORTED, having enqueued nothing, where it cannot run.
+int dtp_fused_forward(void* x_shards, const void* gamma, const void* W1g, const void* W1u, const void* W2, int M,
+                      int d, int F, int P, int L, int delta, int flush, float eps, void* ybase, void* sbuf,
+                      void* ring, int S, int* counters, DeviceStatus* st, const DevInfo& di, cudaStream_t s) {
+    static bool unavailable[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (unavailable[dev & 63]) return SPTP_ERR_UNSUPPORTED;
+    const int max_pairs = dtp_fused_max_pairs(di.sms);
+    if (max_pairs <= 0) {
+        unavailable[dev & 63] = true;
+        return SPTP_ERR_UNSUPPORTED;
+    }
+    const int f = F / P;
+    const uint64_t es = 2;
+    DtpFusedParams p;
+    std::memset(&p, 0, sizeof(p));
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(M), static_cast<uint64_t>(P)};
+        const uint64_t str[2] = {d * es, static_cast<uint64_t>(M) * d * es};
+        const uint32_t box[3] = {kBK, kBM, 1};
+        if (!encode_map_bf16_nd(&p.mapY, ybase, 3, dims, str, box)) return SPTP_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(f),
+                                  static_cast<uint64_t>(L) * P};
+        const uint64_t str[2] = {d * es, static_cast<uint64_t>(f) * d * es};
+        const uint32_t box[3] = {kBK, kBM, 1};
+        if (!encode_map_bf16_nd(&p.mapW1g, W1g, 3, dims, str, box) ||
+            !encode_map_bf16_nd(&p.mapW1u, W1u, 3, dims, str, box))
+            return SPTP_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(f), static_cast<uint64_t>(M), static_cast<uint64_t>(P)};
+        const uint64_t str[2] = {f * es, static_cast<uint64_t>(M) * f * es};
+        const uint32_t box[3] = {kBK, kBM, 1};
+        if (!encode_map_bf16_nd(&p.mapS, sbuf, 3, dims, str, box)) return SPTP_ERR_CUDA;
+    }
+    {
+        const uint64_t dims[4] = {static_cast<uint64_t>(f), static_cast<uint64_t>(P), static_cast<uint64_t>(d),
+                                  static_cast<uint64_t>(L)};
+        const uint64_t str[3] = {f * es, static_cast<uint64_t>(F) * es, static_cast<uint64_t>(d) * F * es};
+        const uint32_t box[4] = {kBK, 1, kBM, 1};
+        if (!encode_map_bf16_nd(&p.mapW2, W2, 4, dims, str, box)) return SPTP_ERR_CUDA;
+    }
+    p.x = x_shards;
+    p.gamma = gamma;
+    p.y = ybase;
+    p.s = sbuf;
+    p.ring = ring;
+    p.eps = eps;
+    p.M = M;
+    p.d = d;
+    p.P = P;
+    p.f = f;
+    p.L = L;
+    p.delta = delta;
+    p.flush = flush ? 1 : 0;
+    p.S = S;
+    p.mt = (M + 255) / 256;
+    p.nt_gu = (f + kBNSwiGLU - 1) / kBNSwiGLU;
+    p.nt_dn = (d + kBNStore - 1) / kBNStore;
+    p.nk_gu = (d + kBK - 1) / kBK;
+    p.nk_dn = (f + kBK - 1) / kBK;
+    p.tiles_per_lm = P * (p.nt_gu + p.nt_dn);
+    p.total_tiles = L * p.mt * p.tiles_per_lm;
+    p.rb_ready = counters;
+    p.gu_done = counters + static_cast<size_t>(L) * p.mt;
+    p.dn_done = p.gu_done + static_cast<size_t>(L) * P * p.mt;
+    p.status = st;
+    p.wait_limit_ns = kWaitLimitNs;
+    const int pairs = p.total_tiles < max_pairs ? p.total_tiles : max_pairs;
+    // a block's down tiles come about one wave of tiles after its gate/up
+    // tiles; the lag stays below the blocks of one module (and of the stack)
+    int lag = (pairs + p.tiles_per_lm - 1) / p.tiles_per_lm + 1;
+    if (lag > p.mt - 1) lag = p.mt - 1;
+    if (lag > L * p.mt - 1) lag = L * p.mt - 1;
+    p.lag = lag < 0 ? 0 : lag;
+    if (cudaMemsetAsync(counters, 0, dtp_counter_bytes(M, P, L), s) != cudaSuccess) return SPTP_ERR_CUDA;
+    const cudaError_t e = launch_dtp_fused(p, pairs, s);
+    if (e == cudaSuccess) return SPTP_OK;
+    cudaGetLastError();
+    if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidValue || e == cudaErrorNotSupported ||
+        e == cudaErrorInvalidConfiguration) {
+        unavailable[dev & 63] = true;
+        return SPTP_ERR_UNSUPPORTED;
+    }
+    return SPTP_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -450,6 +564,7 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
     if (dtype == SPTP_BF16 && gemm_variant() == Variant::kFused) {
         rc = fused_forward(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, out, resid_out, y, sbuf,
                            counters, ws_status(workspace), band, di, s);
+        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
         if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: the three-launch path below
     }
 
@@ -486,7 +601,7 @@ size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta
     const size_t S = static_cast<size_t>(delta + 1 < L ? delta + 1 : L);
     const size_t act = static_cast<size_t>(M) * d * es;
     return SPTP_WS_HEADER_BYTES + align_up(act * P) + align_up(static_cast<size_t>(M) * F * es) +
-           align_up(S * P * act);
+           align_up(S * P * act) + align_up(dtp_counter_bytes(M, P, L));
 }
 
 int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, const void* W1u, const void* W2,
@@ -522,6 +637,13 @@ int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, co
     char* ybase = mptr(workspace, SPTP_WS_HEADER_BYTES);
     char* sbuf = ybase + align_up(act * P);
     char* ring = sbuf + align_up(static_cast<size_t>(M) * F * es);
+    int* counters = reinterpret_cast<int*>(ring + align_up(static_cast<size_t>(S) * P * act));
+    if (dtype == SPTP_BF16 && dtp_fused_selected()) {
+        rc = dtp_fused_forward(x_shards, gamma, W1g, W1u, W2, M, d, F, P, L, delta, flush, eps, ybase, sbuf, ring, S,
+                               counters, ws_status(workspace), di, s);
+        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
+        if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: launches per module below
+    }
     auto xs = [&](int p) { return mptr(x_shards, static_cast<size_t>(p) * act); };
     auto yp = [&](int p) { return ybase + static_cast<size_t>(p) * act; };
     auto o = [&](int l, int p) { return ring + (static_cast<size_t>(l % S) * P + p) * act; };

@@ -102,27 +102,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ void red_release_add(int* ctr, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
-}
-
 // OR of `v` over the 128 epilogue threads (named barrier 1).
-__device__ __forceinline__ bool epilogue_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pin, pout;\n\t"
-        "setp.ne.u32 pin, %1, 0;\n\t"
-        "bar.red.or.pred pout, 1, 128, pin;\n\t"
-        "selp.u32 %0, 1, 0, pout;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v))
-        : "memory");
-    return r != 0;
-}
+__device__ __forceinline__ bool epilogue_any(bool v) { return named_barrier_any<1, 128>(v); }
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
@@ -444,7 +425,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                 // this CTA's 128 rows of the s tile are stored: publish them
                 // to the down tiles' TMA loads
                 fence_proxy_async_global();
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                named_barrier_sync<1, 128>();
                 if (warp == 2 && lane == 0) red_release_add(&p.gu_done[tl.g * p.mt + tl.m], 1);
             }
         }

@@ -542,6 +542,24 @@ bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool encode_map_bf16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                        const uint64_t* strides_bytes, const uint32_t* box) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = get_encode_fn();
+    if (fn == nullptr || rank < 2 || rank > 5) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) gs[i] = strides_bytes[i];
+    }
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gd,
+                    gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s) {
     const int total = p.G * p.mt * p.nt;
     if (total == 0) return cudaSuccess;

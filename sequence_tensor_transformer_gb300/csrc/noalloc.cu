@@ -7,7 +7,7 @@
 // declares itself and that every GPU loading the library holds until exit.
 #include <mutex>
 
-#include "../../include/sptp.h"
+#include "sptp.h"
 #include "sptp_internal.h"
 
 namespace {

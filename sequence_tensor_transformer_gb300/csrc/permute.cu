@@ -13,7 +13,7 @@
 // written as zeros; no out-of-range address is formed.
 #include <cuda_bf16.h>
 
-#include "../../include/sptp.h"
+#include "sptp.h"
 #include "sptp_internal.h"
 
 namespace sptp {

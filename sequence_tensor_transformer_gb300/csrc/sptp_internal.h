@@ -123,6 +123,38 @@ struct FusedParams {
 int fused_max_pairs(int num_sms);
 cudaError_t launch_boundary_fused(const FusedParams& p, int pairs, cudaStream_t s);
 
+// ---------------------------------------------------------------- fused Delayed-TP stack
+struct DtpFusedParams {
+    CUtensorMap mapY;    // y [P][M][d] as {d, M, P}, box {64, 128, 1}
+    CUtensorMap mapW1g;  // W1g [L][P][f][d] as {d, f, L*P}, box {64, 128, 1}
+    CUtensorMap mapW1u;
+    CUtensorMap mapS;    // s [P][M][f] as {f, M, P}, box {64, 128, 1}
+    CUtensorMap mapW2;   // W2 [L][d][P][f] as {f, P, d, L}, box {64, 1, 128, 1}
+    void* x;             // x_shards [P][M][d], updated in place
+    const void* gamma;   // [L][d]
+    void* y;             // [P][M][d]
+    void* s;             // [P][M][f]
+    void* ring;          // pending partials [S][P][M][d]
+    float eps;
+    int M, d, P, f, L, delta, flush, S;
+    int mt, nt_gu, nt_dn, nk_gu, nk_dn;
+    int tiles_per_lm, total_tiles;
+    int lag;             // blocks between a block's gate/up and down tiles (< mt)
+    int* rb_ready;       // [L][mt]   prologue rows normed (all shards)
+    int* gu_done;        // [L][P][mt] gate/up tile halves stored
+    int* dn_done;        // [L][mt]   down tile halves stored (all shards)
+    DeviceStatus* status;
+    unsigned long long wait_limit_ns;
+};
+
+int dtp_fused_max_pairs(int num_sms);
+cudaError_t launch_dtp_fused(const DtpFusedParams& p, int pairs, cudaStream_t s);
+
+// Encodes a rank-N bf16 tensor map (dims innermost first, strides in bytes
+// for dims 1..N-1) with 128-byte swizzle.
+bool encode_map_bf16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                        const uint64_t* strides_bytes, const uint32_t* box);
+
 // ---------------------------------------------------------------- fp32 SIMT GEMM
 struct SimtGemmParams {
     const float* A[kMaxGroups];

@@ -103,6 +103,27 @@ __device__ __forceinline__ bool flag_wait_geq(const int* flag, int target, const
     }
 }
 
+// Warp-wide bounded wait until a global int reaches `target`: every lane
+// performs its own acquire load of the same word (one transaction, so every
+// lane sees the same value and the loop stays warp-uniform), so each lane's
+// later reads are ordered after the releasing writes.  Returns false if the
+// wait gave up.
+__device__ __forceinline__ bool warp_flag_wait_geq(const int* flag, int target, const WaitCtx& w, int where,
+                                                   int info) {
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (__all_sync(0xffffffffu, v >= target)) return true;
+        if (__any_sync(0xffffffffu, *w.abort_flag != 0)) return false;
+        if (__any_sync(0xffffffffu, global_timer_ns() - t0 > w.limit_ns)) {
+            if ((threadIdx.x & 31) == 0) report_timeout(w, where, info);
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -133,6 +154,27 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
 // async-proxy (TMA) accesses of shared memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 3-D and 4-D tiled loads for CTA pairs (coordinates innermost first); the
+// shared-memory image of a box with trailing extents of 1 is that of the 2-D
+// box.
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t mbar_cluster,
+                                                 int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(void* smem_dst, const CUtensorMap* map, uint32_t mbar_cluster,
+                                                 int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -189,6 +231,17 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
           "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
           "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Loads 16 consecutive fp32 columns of the warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 }
@@ -266,6 +319,35 @@ __device__ __forceinline__ void umma_commit_pair_multicast(uint64_t* bar, uint16
             smem_u32(bar)),
         "h"(cta_mask)
         : "memory");
+}
+
+// ---------------------------------------------------------------- cross-CTA publication
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_release_add(int* ctr, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+// OR of `v` over the `nthreads` threads that use named barrier `id`.
+template <int ID, int NTHREADS>
+__device__ __forceinline__ bool named_barrier_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.or.pred pout, %2, %3, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(ID), "n"(NTHREADS)
+        : "memory");
+    return r != 0;
+}
+
+template <int ID, int NTHREADS>
+__device__ __forceinline__ void named_barrier_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(NTHREADS) : "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with

@@ -8,6 +8,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+# a fused variant named by a test must be the one that runs (no fall-back)
+os.environ.setdefault("SPTP_STRICT_VARIANT", "1")
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
 

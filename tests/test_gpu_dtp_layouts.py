@@ -14,6 +14,14 @@ from helpers import TOL, dev_tensor, host_f64, rel_err, to_f64
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["fused", "layers"])
+def dtp_variant(request, monkeypatch):
+    """Delayed-TP stack as one fused persistent launch (default) or as a
+    prologue and two GEMM launches per module."""
+    monkeypatch.setenv("SPTP_DTP_VARIANT", request.param)
+    return request.param
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     if not torch.cuda.is_available():
@@ -76,7 +84,7 @@ def run_permuted_dtp(cfg, perms, flush, rows=None):
     return got, ref
 
 
-def test_permuted_dtp_stack_workload_sampled_rows():
+def test_permuted_dtp_stack_workload_sampled_rows(dtp_variant):
     cfg = synth.DTP_STACK
     rows = [0, 1, 77, 1024, 2047, 3333, 4095]
     got, ref = run_permuted_dtp(cfg, _perms(cfg.L, cfg.F, 11), 1, rows=rows)
@@ -85,7 +93,7 @@ def test_permuted_dtp_stack_workload_sampled_rows():
 
 
 @pytest.mark.parametrize("P,L,delta,flush", [(2, 3, 1, 0), (3, 2, 0, 1), (4, 3, 2, 1)])
-def test_permuted_dtp_small_cases(P, L, delta, flush):
+def test_permuted_dtp_small_cases(P, L, delta, flush, dtp_variant):
     cfg = synth.DTPConfig("perm", 160, 136, P * 48, P, L, delta, "bf16")
     got, ref = run_permuted_dtp(cfg, _perms(L, cfg.F, P + L), flush)
     for p in range(P):

@@ -15,6 +15,14 @@ from helpers import TOL, dev_tensor, host_f64, rel_err, to_f64
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["fused", "layers"])
+def dtp_variant(request, monkeypatch):
+    """Delayed-TP stack as one fused persistent launch (default) or as a
+    prologue and two GEMM launches per module."""
+    monkeypatch.setenv("SPTP_DTP_VARIANT", request.param)
+    return request.param
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     if not torch.cuda.is_available():
@@ -236,7 +244,7 @@ def run_dtp(cfg, flush=1, independent=False, rows=None):
     return got, ref
 
 
-def test_dtp_stack_config_full_size_sampled_rows():
+def test_dtp_stack_config_full_size_sampled_rows(dtp_variant):
     cfg = synth.DTP_STACK
     for flush in (0, 1):
         got, ref = run_dtp(cfg, flush=flush, rows=sample_rows(cfg.M, 32))
@@ -246,7 +254,7 @@ def test_dtp_stack_config_full_size_sampled_rows():
 
 @pytest.mark.parametrize("P,L,delta,flush,indep", [(2, 3, 0, 1, False), (3, 4, 2, 0, True), (4, 2, 5, 1, False),
                                                    (1, 3, 1, 1, False), (2, 5, 1, 0, False)])
-def test_dtp_small_cases(P, L, delta, flush, indep):
+def test_dtp_small_cases(P, L, delta, flush, indep, dtp_variant):
     cfg = synth.DTPConfig("t", 200, 136, P * 48, P, L, delta, "bf16")
     got, ref = run_dtp(cfg, flush=flush, independent=indep)
     for p in range(P):
@@ -260,7 +268,7 @@ def test_dtp_fp32():
         assert rel_err(got[p], ref[p]) <= TOL["fp32"], p
 
 
-def test_dtp_delta0_equals_chained_boundaries_on_gpu():
+def test_dtp_delta0_equals_chained_boundaries_on_gpu(dtp_variant):
     cfg = synth.DTPConfig("t0", 256, 256, 2 * 256, 2, 3, 0, "bf16")
     inp = synth.dtp_inputs(cfg)
     T = {k: dev_tensor(v, "bf16") for k, v in inp.items()}
