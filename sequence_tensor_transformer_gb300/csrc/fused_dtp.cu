@@ -3,7 +3,7 @@
 // the other devices' partials delta modules later).
 //
 // One cooperative launch of CTA pairs runs all L modules of the stack:
-//   warps 6..13   prologue: rows in the order (module step l = 0..L, 256-row
+//   warps 6..11   prologue: rows in the order (module step l = 0..L, 256-row
 //                 block m, shard p, row); row r of shard p at step l waits
 //                 (bounded) until step l-1's down tiles of block m are stored,
 //                 then x_p[r] += own partial of module l-1 + the other shards'
@@ -48,7 +48,7 @@ constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 4;
-constexpr int PRO_WARPS = 8;
+constexpr int PRO_WARPS = 6;
 constexpr int PRO_WARP0 = 2 + EPI_WARPS;
 constexpr int THREADS = 32 * (2 + EPI_WARPS + PRO_WARPS);
 constexpr uint32_t IDESC = idesc_bf16_f32(PBM, PBN);
@@ -142,58 +142,93 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Columns of one row handled per batch: lane l owns the 16-byte vectors at
-// columns base + 8*l + 256*v, v < kRowVec, i.e. 512 columns per batch (two
-// vectors per source keep the kernel within its register budget).
-constexpr int kRowVec = 2;
+// columns base + 8*l + 256*v, v < kRowVec, i.e. 1024 columns per batch.
+constexpr int kRowVec = 4;
 
-// Adds one source's batch (kRowVec vectors of 8 columns) into acc.
-__device__ __forceinline__ void add_batch(const __nv_bfloat16* src, long long off, int col0, int d,
-                                          float (&acc)[kRowVec][8]) {
-    uint4 u[kRowVec];
-#pragma unroll
-    for (int v = 0; v < kRowVec; ++v)
-        if (col0 + 256 * v < d) u[v] = *reinterpret_cast<const uint4*>(src + off + 256 * v);
-#pragma unroll
-    for (int v = 0; v < kRowVec; ++v) {
-        if (col0 + 256 * v < d) {
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[v]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f2 = __bfloat1622float2(h2[i]);
-                acc[v][2 * i] += f2.x;
-                acc[v][2 * i + 1] += f2.y;
-            }
-        }
-    }
+// Number of partial sources added into shard sh's stream at step l, and
+// the j-th of them, in the canonical order: own partial of module l-1; the
+// other shards' partials of module l-1-delta (ascending shard); at the final
+// flushing step the still-pending ones (module-major, ascending shard).
+__device__ __forceinline__ int n_sources(const DtpFusedParams& p, int l) {
+    int n = l >= 1 ? 1 : 0;
+    if (l - 1 - p.delta >= 0) n += p.P - 1;
+    if (l == p.L && p.flush) n += (p.P - 1) * (p.L - (p.L - p.delta > 0 ? p.L - p.delta : 0));
+    return n;
 }
 
-// h for one batch of a row of shard `sh` at step l: x + (0 + own partial of
-// module l-1 + other shards' partials of module l-1-delta (ascending shard) +
-// at the final flushing step the still-pending ones (module-major, ascending
-// shard)) -- the order of the three-launch path's source list.  h first
-// accumulates the sources, then x is added.
+__device__ __forceinline__ const __nv_bfloat16* source_j(const DtpFusedParams& p, int l, int sh, int j) {
+    const long long act = static_cast<long long>(p.M) * p.d;
+    const __nv_bfloat16* ring = static_cast<const __nv_bfloat16*>(p.ring);
+    int module, q;
+    if (l >= 1 && j == 0) {
+        module = l - 1;
+        q = sh;
+    } else {
+        if (l >= 1) --j;
+        const int n_oth = (l - 1 - p.delta >= 0) ? p.P - 1 : 0;
+        int idx;
+        if (j < n_oth) {
+            module = l - 1 - p.delta;
+            idx = j;
+        } else {
+            j -= n_oth;
+            module = (p.L - p.delta > 0 ? p.L - p.delta : 0) + j / (p.P - 1);
+            idx = j % (p.P - 1);
+        }
+        q = idx < sh ? idx : idx + 1;
+    }
+    return ring + (static_cast<long long>(module % p.S) * p.P + q) * act;
+}
+
+// h for one batch of a row of shard `sh` at step l: x + (0 + s_0 + s_1 +
+// ...), the sources in the order above -- the three-launch path's order.
+// Loads are issued three sources (x counting as the last one) at a time, so a
+// row with up to two partial sources costs one round of loads.
+constexpr int kSrcBatch = 3;
+
 __device__ __forceinline__ void step_h(const DtpFusedParams& p, int l, int sh, long long row, int base, int lane,
                                        float (&h)[kRowVec][8]) {
     const long long act = static_cast<long long>(p.M) * p.d;
-    const __nv_bfloat16* ring = static_cast<const __nv_bfloat16*>(p.ring);
     const long long off = row * p.d + base + lane * 8;
     const int col0 = base + lane * 8;
+    const int ns = n_sources(p, l);
 #pragma unroll
     for (int v = 0; v < kRowVec; ++v)
 #pragma unroll
         for (int e = 0; e < 8; ++e) h[v][e] = 0.f;
-    if (l >= 1) add_batch(ring + (static_cast<long long>((l - 1) % p.S) * p.P + sh) * act, off, col0, p.d, h);
-    const int k = l - 1 - p.delta;
-    if (k >= 0)
-        for (int q = 0; q < p.P; ++q)
-            if (q != sh) add_batch(ring + (static_cast<long long>(k % p.S) * p.P + q) * act, off, col0, p.d, h);
-    if (l == p.L && p.flush)
-        for (int kk = (p.L - p.delta > 0 ? p.L - p.delta : 0); kk < p.L; ++kk)
-            for (int q = 0; q < p.P; ++q)
-                if (q != sh)
-                    add_batch(ring + (static_cast<long long>(kk % p.S) * p.P + q) * act, off, col0, p.d, h);
-    // + x last (one IEEE addition per element, so h + x == x + h bit for bit)
-    add_batch(static_cast<const __nv_bfloat16*>(p.x) + sh * act, off, col0, p.d, h);
+    for (int j0 = 0; j0 <= ns; j0 += kSrcBatch) {
+        uint4 u[kSrcBatch][kRowVec];
+#pragma unroll
+        for (int jj = 0; jj < kSrcBatch; ++jj) {
+            const int j = j0 + jj;
+            if (j <= ns) {
+                const __nv_bfloat16* src =
+                    (j == ns ? static_cast<const __nv_bfloat16*>(p.x) + sh * act : source_j(p, l, sh, j)) + off;
+#pragma unroll
+                for (int v = 0; v < kRowVec; ++v)
+                    if (col0 + 256 * v < p.d) u[jj][v] = *reinterpret_cast<const uint4*>(src + 256 * v);
+            }
+        }
+        // in order: the sources, then x (one IEEE addition each, so h + x ==
+        // x + h bit for bit)
+#pragma unroll
+        for (int jj = 0; jj < kSrcBatch; ++jj) {
+            if (j0 + jj <= ns) {
+#pragma unroll
+                for (int v = 0; v < kRowVec; ++v) {
+                    if (col0 + 256 * v < p.d) {
+                        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[jj][v]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 f2 = __bfloat1622float2(h2[i]);
+                            h[v][2 * i] += f2.x;
+                            h[v][2 * i + 1] += f2.y;
+                        }
+                    }
+                }
+            }
+        }
+    }
 }
 
 // Writes one batch of the row: x_p <- h, and y_p <- h * inv * gamma_l (l < L).
