@@ -7,8 +7,8 @@
 //
 // HBM-bound gathers, every byte read and written once:
 //   rows    W1g/W1u: one warp per output row, 16-byte coalesced copies
-//   columns W2: one CTA per output row; the input row is staged in shared
-//           memory and gathered into coalesced stores
+//   columns W2: a CTA stages up to 8 whole rows in shared memory with
+//           16-byte loads and writes the gathered rows with 16-byte stores
 // An index outside [0, F) is recorded in the status words and its output is
 // written as zeros; no out-of-range address is formed.
 #include <cuda_bf16.h>
@@ -56,27 +56,47 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t* in0, c
     }
 }
 
-// out[l][r][i] = in[l][r][perm[l][i]]; one CTA per (l, r) row, rows of F
-// elements of `es` bytes staged in shared memory
-template <typename T>
+// out[l][r][i] = in[l][r][perm[l][i]]: a CTA stages ROWS consecutive rows of
+// one module in shared memory with 16-byte loads, then each thread gathers 16
+// bytes' worth of consecutive output elements and writes them with one
+// 16-byte store (F * sizeof(T) is a multiple of 16).
+template <typename T, int ROWS>
 __global__ void __launch_bounds__(512) permute_cols_kernel(const T* in, T* out, const int* perm, int L, int R, int F,
                                                            DeviceStatus* st) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    T* row = reinterpret_cast<T*>(smem_raw);
-    const long long rows = static_cast<long long>(L) * R;
-    for (long long lr = blockIdx.x; lr < rows; lr += gridDim.x) {
-        const int l = static_cast<int>(lr / R);
-        const T* src = in + lr * F;
-        T* dst = out + lr * F;
+    T* rows_s = reinterpret_cast<T*>(smem_raw);
+    constexpr int E = 16 / sizeof(T);  // elements per 16-byte vector
+    const int vec_per_row = F / E;
+    const long long groups = static_cast<long long>(L) * ((R + ROWS - 1) / ROWS);
+    const int gpl = (R + ROWS - 1) / ROWS;  // row groups per module
+    for (long long gi = blockIdx.x; gi < groups; gi += gridDim.x) {
+        const int l = static_cast<int>(gi / gpl);
+        const int r0 = static_cast<int>(gi - static_cast<long long>(l) * gpl) * ROWS;
+        const int nr = min(ROWS, R - r0);
+        const T* src = in + (static_cast<long long>(l) * R + r0) * F;
+        T* dst = out + (static_cast<long long>(l) * R + r0) * F;
         const int* pl = perm + static_cast<long long>(l) * F;
-        __syncthreads();  // previous row fully gathered
-        for (int i = threadIdx.x; i < F; i += blockDim.x) row[i] = src[i];
+        __syncthreads();  // the previous group is fully gathered
+#pragma unroll 4
+        for (int v = threadIdx.x; v < nr * vec_per_row; v += blockDim.x)
+            reinterpret_cast<uint4*>(rows_s)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
         __syncthreads();
-        for (int i = threadIdx.x; i < F; i += blockDim.x) {
-            const int s = pl[i];
-            const bool ok = s >= 0 && s < F;
-            if (!ok && (lr % R) == 0) report_bad_index(st, i);
-            dst[i] = ok ? row[s] : T(0);
+#pragma unroll 2
+        for (int v = threadIdx.x; v < nr * vec_per_row; v += blockDim.x) {
+            const int r = v / vec_per_row;
+            const int i0 = (v - r * vec_per_row) * E;
+            union {
+                uint4 u;
+                T e[E];
+            } pack;
+#pragma unroll
+            for (int k = 0; k < E; ++k) {
+                const int sidx = pl[i0 + k];
+                const bool ok = sidx >= 0 && sidx < F;
+                if (!ok && r0 + r == 0) report_bad_index(st, i0 + k);
+                pack.e[k] = ok ? rows_s[static_cast<long long>(r) * F + sidx] : T(0);
+            }
+            reinterpret_cast<uint4*>(dst)[v] = pack.u;
         }
     }
 }
@@ -96,23 +116,34 @@ cudaError_t launch_permute_ffn(const void* W1g, const void* W1u, const void* W2,
         static_cast<uint8_t*>(W1u_out), perm, L, F, d * es, st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t smem = static_cast<size_t>(F) * es;
-    long long grid2 = static_cast<long long>(L) * d;
+    // as many whole rows per CTA as fit in ~96 KiB of shared memory (<= 8)
+    int rpc = static_cast<int>((96u * 1024u) / (static_cast<size_t>(F) * es));
+    rpc = rpc >= 8 ? 8 : (rpc >= 4 ? 4 : (rpc >= 2 ? 2 : 1));
+    const size_t smem = static_cast<size_t>(rpc) * F * es;
+    long long grid2 = static_cast<long long>(L) * ((d + rpc - 1) / rpc);
     if (grid2 > static_cast<long long>(num_sms) * 4) grid2 = static_cast<long long>(num_sms) * 4;
+    auto launch = [&](auto kfn, auto tag) -> cudaError_t {
+        using TT = decltype(tag);
+        cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        kfn<<<static_cast<int>(grid2), 512, smem, s>>>(static_cast<const TT*>(W2), static_cast<TT*>(W2_out), perm, L,
+                                                        d, F, st);
+        return cudaGetLastError();
+    };
     if (bf16) {
-        e = cudaFuncSetAttribute(permute_cols_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        permute_cols_kernel<__nv_bfloat16><<<static_cast<int>(grid2), 512, smem, s>>>(
-            static_cast<const __nv_bfloat16*>(W2), static_cast<__nv_bfloat16*>(W2_out), perm, L, d, F, st);
-    } else {
-        e = cudaFuncSetAttribute(permute_cols_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        permute_cols_kernel<float><<<static_cast<int>(grid2), 512, smem, s>>>(
-            static_cast<const float*>(W2), static_cast<float*>(W2_out), perm, L, d, F, st);
+        switch (rpc) {
+            case 8: return launch(permute_cols_kernel<__nv_bfloat16, 8>, __nv_bfloat16());
+            case 4: return launch(permute_cols_kernel<__nv_bfloat16, 4>, __nv_bfloat16());
+            case 2: return launch(permute_cols_kernel<__nv_bfloat16, 2>, __nv_bfloat16());
+            default: return launch(permute_cols_kernel<__nv_bfloat16, 1>, __nv_bfloat16());
+        }
     }
-    return cudaGetLastError();
+    switch (rpc) {
+        case 8: return launch(permute_cols_kernel<float, 8>, float());
+        case 4: return launch(permute_cols_kernel<float, 4>, float());
+        case 2: return launch(permute_cols_kernel<float, 2>, float());
+        default: return launch(permute_cols_kernel<float, 1>, float());
+    }
 }
 
 }  // namespace sptp
