@@ -316,6 +316,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier(pg, dev)
     ms_total = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    out_ref, resid_ref = out.clone(), resid.clone()  # the timed call's results
     ms_step = ms_total / args.steps
     fl = flops_per_step(cfg)
     value = fl * world / (ms_step * 1e-3) / 1e12
@@ -439,8 +440,9 @@ def run_ours(args):
     t_end.record(s_out)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(pg, t_start.elapsed_time(t_end), dev) / n_e
-    # the pipeline's results match the device-resident run
-    assert torch.equal(out_h, out.cpu()) and torch.equal(res_h, resid.cpu())
+    # the pipeline's results match the device-resident run of the same call
+    assert torch.equal(out_h, out_ref.cpu()) and torch.equal(res_h, resid_ref.cpu())
+    del out_ref, resid_ref
     h2d = (pin_x.numel() + pin_p.numel()) * 2
     d2h = (out_h.numel() + res_h.numel()) * 2
     e2e = {"value": fl * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,

@@ -91,10 +91,11 @@ constexpr int kBM = 128, kBNSwiGLU = 128, kBNStore = 256, kBK = 64;
 //   "fused"          the whole boundary in one persistent CTA-pair launch
 //                    (falls back to "pair" where it cannot be launched)
 //   "single"         prologue + single-CTA gate/up + down launches
-// The step-level entry points use "pair" unless "single" is selected.  The
-// fused launch needs about 5% fewer SM cycles per boundary but, under the
-// GPU's power cap, ran at a lower clock and measured ~1.5% slower than
-// "pair" on the 8192 x 4096 x 14336 boundary, so "pair" is the default.
+// The step-level entry points use "pair" unless "single" is selected.  On the
+// 8192 x 4096 x 14336 boundary the fused launch and "pair" measure level
+// (1670-1675 vs 1668-1669 TFLOP/s); the fused one needs ~7% fewer SM cycles
+// but, under the GPU's power cap, runs at a lower clock.  "pair" stays the
+// default: its kernels can be profiled with ncu, the cooperative launch not.
 enum class Variant { kFused, kPair, kSingle };
 
 Variant gemm_variant() {
@@ -368,8 +369,8 @@ int fused_forward(const void* x, const void* partials, const void* gamma, const 
     // First gate/up band: 2048 rows, or one sequence chunk if taller.  The
     // first wave waits for these rows from the prologue warps; a shorter band
     // starts sooner but streams the weights once more.  (Measured on the
-    // 8192 x 4096 x 14336 boundary: first bands of 1024 / 2048 / 4096 rows
-    // gave 1594 / 1635 / 1569 TFLOP/s.)
+    // 8192 x 4096 x 14336 boundary: first bands of 2048 / 4096 rows gave
+    // 1670-1675 / 1638-1639 TFLOP/s.)
     const int chunk_rows = M / chunks;
     const int first_rows = chunk_rows > kFirstBandRows ? chunk_rows : kFirstBandRows;
     const int first_tiles = first_rows / 256;

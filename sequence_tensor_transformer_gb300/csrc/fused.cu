@@ -132,21 +132,22 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // h = x + (0 + partial_0 + partial_1 + ...) for NV 8-column vectors of one
 // row, 256 columns apart (vectors past d are left untouched); the loads of
-// one source for all NV vectors are issued together.
+// one source for all NV vectors are issued together.  h accumulates the
+// partials first and x last (one IEEE addition per element, so h + x equals
+// x + h bit for bit).
 template <int NV>
 __device__ __forceinline__ void row_h(const FusedParams& p, long long row_off, int col0, float (&h)[NV][8]) {
-    float r[NV][8];
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) r[v][e] = 0.f;
-    for (int q = 0; q < p.P; ++q) {
+        for (int e = 0; e < 8; ++e) h[v][e] = 0.f;
+    for (int q = 0; q <= p.P; ++q) {
+        const __nv_bfloat16* src = q < p.P ? static_cast<const __nv_bfloat16*>(p.partials[q])
+                                           : static_cast<const __nv_bfloat16*>(p.x);
         uint4 u[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v)
-            if (col0 + 256 * v < p.d)
-                u[v] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.partials[q]) +
-                                                            row_off + col0 + 256 * v));
+            if (col0 + 256 * v < p.d) u[v] = __ldg(reinterpret_cast<const uint4*>(src + row_off + col0 + 256 * v));
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             if (col0 + 256 * v < p.d) {
@@ -154,18 +155,10 @@ __device__ __forceinline__ void row_h(const FusedParams& p, long long row_off, i
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 f2 = __bfloat1622float2(h2[i]);
-                    r[v][2 * i] += f2.x;
-                    r[v][2 * i + 1] += f2.y;
+                    h[v][2 * i] += f2.x;
+                    h[v][2 * i + 1] += f2.y;
                 }
             }
-        }
-    }
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        if (col0 + 256 * v < p.d) {
-            load8(static_cast<const __nv_bfloat16*>(p.x) + row_off + col0 + 256 * v, h[v]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) h[v][e] += r[v][e];
         }
     }
 }
@@ -227,7 +220,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
         for (long long row = static_cast<long long>(blockIdx.x) * PRO_WARPS + (warp - 6); row < p.M; row += W) {
             if (*wc.abort_flag) break;
             const long long base = row * d;
-            constexpr int NV = 2;
+            constexpr int NV = 4;
             float ss = 0.f;
             for (int col0 = lane * 8; col0 < d; col0 += 256 * NV) {
                 float h[NV][8];
@@ -376,14 +369,14 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                 __nv_bfloat16* out =
                     reinterpret_cast<__nv_bfloat16*>(p.s_out[tl.g]) + static_cast<long long>(row) * p.f;
 #pragma unroll 1
-                for (int c = 0; c < PBN / 2; c += 32) {
-                    uint32_t gv[32], uv[32];
-                    tmem_ld_32cols(taddr + c, gv);
-                    tmem_ld_32cols(taddr + PBN / 2 + c, uv);
+                for (int c = 0; c < PBN / 2; c += 16) {
+                    uint32_t gv[16], uv[16];
+                    tmem_ld_16cols(taddr + c, gv);
+                    tmem_ld_16cols(taddr + PBN / 2 + c, uv);
                     tmem_ld_wait();
-                    uint32_t packed[16];
+                    uint32_t packed[8];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 8; ++j) {
                         const float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
                         const float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
                         packed[j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
@@ -391,7 +384,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     const int col = tl.n * (PBN / 2) + c;
                     if (row_ok) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
+                        for (int v = 0; v < 2; ++v)
                             if (col + 8 * v < p.f)
                                 *reinterpret_cast<uint4*>(out + col + 8 * v) =
                                     make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
@@ -401,18 +394,18 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                 __nv_bfloat16* out =
                     reinterpret_cast<__nv_bfloat16*>(p.out[tl.g]) + static_cast<long long>(row) * p.d;
 #pragma unroll 1
-                for (int c = 0; c < PBN; c += 32) {
-                    uint32_t v32[32];
-                    tmem_ld_32cols(taddr + c, v32);
+                for (int c = 0; c < PBN; c += 16) {
+                    uint32_t v16[16];
+                    tmem_ld_16cols(taddr + c, v16);
                     tmem_ld_wait();
-                    uint32_t packed[16];
+                    uint32_t packed[8];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        packed[j] = pack_bf16x2(__uint_as_float(v32[2 * j]), __uint_as_float(v32[2 * j + 1]));
+                    for (int j = 0; j < 8; ++j)
+                        packed[j] = pack_bf16x2(__uint_as_float(v16[2 * j]), __uint_as_float(v16[2 * j + 1]));
                     const int col = tl.n * PBN + c;
                     if (row_ok) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
+                        for (int v = 0; v < 2; ++v)
                             if (col + 8 * v < p.d)
                                 __stcs(reinterpret_cast<uint4*>(out + col + 8 * v),
                                        make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
