@@ -1,0 +1,173 @@
+"""Oracle for the fp8 (E4M3) variant of the SP-TP FFN boundary.
+
+TEST INFRASTRUCTURE ONLY: a plain float64 CPU statement of what the fp8 path
+of the CUDA library computes.  Only the tests, the package smoke check and the
+benchmark's CPU legs may import it; the product path never calls it.
+
+Source (web page; title and section): "[Feature] Async Tensor Parallelism for
+Archon Engine", section "Additional Information" names fp8 (MXFP8) linear
+layers inside tensor-parallel blocks as a known limitation; it fixes no
+scaling recipe.  Readings taken here, each also listed in the repository's
+design notes:
+
+* Every linear layer's input is the bf16 activation (y after RMSNorm, s after
+  SwiGLU), as in a bf16 model whose linears run in fp8; the layer quantises
+  that bf16 tensor itself.
+* Quantisation is row-wise with power-of-two scales: a row r of a [R][K]
+  operand (K the reduction axis) gets e_r = the smallest integer >= -126 with
+  max_k |a[r][k]| <= 448 * 2^e_r; its codes are q[r][k] = RNE_E4M3(a[r][k] *
+  2^-e_r).  A power of two makes a * 2^-e exact, so any implementation that
+  quantises the same bf16 value takes the same decision.  (MX formats share
+  one power-of-two scale per 32 elements; one scale per row is the plainest
+  scaling that a GEMM epilogue can undo exactly.)
+* Scale axes: y per token row over d; W1g and W1u per output neuron (row of
+  [F][d]) over d; s per token row over the shard's F/P neurons; W2 per output
+  feature n and shard p over W2[n][F_p].  Shard p's scales are its own: a
+  real TP rank quantises its local shard.
+* A GEMM of quantised operands is sum_k qa qb times 2^(e_a + e_b); gate and
+  up values are dequantised before SwiGLU.
+
+Parity status: round_bf16 and round_e4m3 are pinned against PyTorch's casts;
+e4m3_row_exponent by closed forms and minimality; the composition by a
+hand-derived worked example, exact power-of-two equivariances and an error
+bound against the float64 boundary.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .sptp_oracle import reduce_partials, rms_norm, silu
+
+E4M3_MAX = 448.0
+MIN_EXPONENT = -126
+
+
+def _round_to_grid(v: np.ndarray, significant_bits: int, min_normal_exp: int) -> np.ndarray:
+    """Round-to-nearest-even onto a binary floating-point grid with
+    `significant_bits` bits of significand (implicit bit included) and
+    smallest normal binade [2^min_normal_exp, 2^(min_normal_exp+1)); below it
+    the spacing stays that of the smallest binade (subnormals)."""
+    v = np.asarray(v, dtype=np.float64)
+    _, ex = np.frexp(v)  # v = m * 2^ex, 0.5 <= |m| < 1, so the leading bit is 2^(ex-1)
+    lead = np.maximum(ex - 1, min_normal_exp)
+    ulp = np.ldexp(1.0, lead - (significant_bits - 1))
+    return np.rint(v / ulp) * ulp
+
+
+def round_bf16(v) -> np.ndarray:
+    """Round to bfloat16 (8 significant bits, float32's exponent range),
+    nearest-even; values past the largest finite bf16 become +-inf."""
+    r = _round_to_grid(v, 8, -126)
+    big = np.abs(r) >= 2.0 ** 128
+    return np.where(big, np.copysign(np.inf, r), r)
+
+
+def round_e4m3(v) -> np.ndarray:
+    """Round to OCP E4M3 (4 significant bits, exponent bias 7, smallest normal
+    2^-6, subnormal spacing 2^-9, largest finite 448), nearest-even.  Inputs
+    whose rounding leaves [-448, 448] are outside the domain used here."""
+    r = _round_to_grid(v, 4, -6)
+    if np.any(np.abs(r) > E4M3_MAX):
+        raise ValueError("value outside the E4M3 range")
+    return r
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Byte encoding of values on the E4M3 grid: sign << 7 | exponent field
+    << 3 | mantissa, exponent field 0 for zero and subnormals."""
+    v = np.asarray(v, dtype=np.float64)
+    if not np.array_equal(round_e4m3(v), v):
+        raise ValueError("value not on the E4M3 grid")
+    a = np.abs(v)
+    sign = np.signbit(v).astype(np.int64)
+    _, ex = np.frexp(a)
+    lead = ex - 1
+    normal = a >= 2.0 ** -6
+    field = np.where(normal, lead + 7, 0)
+    mant = np.where(normal, np.ldexp(a, -lead) * 8 - 8, a * 2.0 ** 9)
+    code = (sign << 7) | (field.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
+    return code.astype(np.uint8)
+
+
+def e4m3_row_exponent(amax) -> np.ndarray:
+    """Smallest integer e >= -126 with amax <= 448 * 2^e (elementwise)."""
+    amax = np.asarray(amax, dtype=np.float64)
+    out = np.empty(amax.shape, dtype=np.int64)
+    for i, a in np.ndenumerate(amax):
+        e = MIN_EXPONENT
+        while a > E4M3_MAX * 2.0 ** e:
+            e += 1
+        out[i] = e
+    return out
+
+
+def quantize_rows_e4m3(a):
+    """Row-wise power-of-two-scaled E4M3 quantisation over the last axis.
+    Returns (q, e): q the E4M3 values (float64, on the grid), e the int
+    exponents, a ~= q * 2^e[..., None]."""
+    a = np.asarray(a, dtype=np.float64)
+    e = e4m3_row_exponent(np.max(np.abs(a), axis=-1) if a.shape[-1] else np.zeros(a.shape[:-1]))
+    q = round_e4m3(a * np.ldexp(1.0, -e)[..., None])
+    return q, e
+
+
+def quantize_ffn_weights(W1g, W1u, W2, P: int):
+    """The fp8 weights of one FFN: W1g/W1u per neuron row over d, W2 per
+    (output feature n, shard p) over W2[n][F_p].  Returns
+    (qg, eg, qu, eu, q2, e2) with e2 of shape [d, P]."""
+    W1g = np.asarray(W1g, dtype=np.float64)
+    W1u = np.asarray(W1u, dtype=np.float64)
+    W2 = np.asarray(W2, dtype=np.float64)
+    d, F = W2.shape
+    f = F // P
+    qg, eg = quantize_rows_e4m3(W1g)
+    qu, eu = quantize_rows_e4m3(W1u)
+    q2, e2 = quantize_rows_e4m3(W2.reshape(d, P, f))
+    return qg, eg, qu, eu, q2.reshape(d, F), e2
+
+
+def shard_ffn_fp8(y, qw, P: int, p: int, return_intermediates: bool = False):
+    """Shard p's fp8 gate/up GEMM, SwiGLU and fp8 down GEMM on bf16 rows y
+    [R][d]; qw = quantize_ffn_weights(...).  Returns the partial [R][d]
+    (float64, before any output rounding)."""
+    qg, eg, qu, eu, q2, e2 = qw
+    F = qg.shape[0]
+    f = F // P
+    n = slice(p * f, (p + 1) * f)
+    qy, ey = quantize_rows_e4m3(y)
+    sy = np.ldexp(1.0, ey)[:, None]
+    a = (qy @ qg[n].T) * sy * np.ldexp(1.0, eg[n])[None, :]
+    b = (qy @ qu[n].T) * sy * np.ldexp(1.0, eu[n])[None, :]
+    s = round_bf16(silu(a) * b)
+    qs, es = quantize_rows_e4m3(s)
+    out = (qs @ q2[:, n].T) * np.ldexp(1.0, es)[:, None] * np.ldexp(1.0, e2[:, p])[None, :]
+    if return_intermediates:
+        return out, dict(qy=qy, ey=ey, a=a, b=b, s=s, qs=qs, es=es)
+    return out
+
+
+def sptp_ffn_forward_fp8(x, partials, gamma, W1g, W1u, W2, P: int, chunks: int, eps: float, rows=None):
+    """The SP-TP FFN boundary with fp8 linear layers: per chunk the P partials
+    are summed, the residual added and the sum RMS-normalised; y is the bf16
+    activation; every shard runs shard_ffn_fp8 on it.  Arguments and return
+    value as in the float64 boundary: (out [P, R, d], h [R, d])."""
+    M, d = x.shape
+    F = W1g.shape[0]
+    if partials.shape[0] != P or F % P != 0 or chunks < 1 or M % chunks != 0:
+        raise ValueError("bad shape")
+    qw = quantize_ffn_weights(W1g, W1u, W2, P)
+    sel = np.arange(M) if rows is None else np.asarray(rows)
+    out = np.zeros((P, len(sel), d))
+    h_out = np.zeros((len(sel), d))
+    m = M // chunks
+    for c in range(chunks):
+        pos = np.nonzero((sel >= c * m) & (sel < (c + 1) * m))[0]
+        if len(pos) == 0:
+            continue
+        r_idx = sel[pos]
+        h = x[r_idx] + reduce_partials(partials[:, r_idx, :])
+        y = round_bf16(rms_norm(h, gamma, eps))
+        h_out[pos] = h
+        for p in range(P):
+            out[p, pos] = shard_ffn_fp8(y, qw, P, p)
+    return out, h_out
