@@ -92,13 +92,13 @@ def e4m3_encode(v) -> np.ndarray:
 def e4m3_row_exponent(amax) -> np.ndarray:
     """Smallest integer e >= -126 with amax <= 448 * 2^e (elementwise)."""
     amax = np.asarray(amax, dtype=np.float64)
-    out = np.empty(amax.shape, dtype=np.int64)
-    for i, a in np.ndenumerate(amax):
-        e = MIN_EXPONENT
-        while a > E4M3_MAX * 2.0 ** e:
-            e += 1
-        out[i] = e
-    return out
+    e = np.full(amax.shape, MIN_EXPONENT, dtype=np.int64)
+    # count upwards from -126 until 448 * 2^e covers amax (every row at once)
+    while True:
+        short = amax > E4M3_MAX * np.ldexp(1.0, e)
+        if not np.any(short):
+            return e
+        e = e + short
 
 
 def quantize_rows_e4m3(a):
