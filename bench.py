@@ -39,9 +39,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["boundary", "dtp", "attn", "permute"], default="boundary",
+    ap.add_argument("--workload", choices=["boundary", "dtp", "attn", "permute", "fp8"], default="boundary",
                     help="boundary: the SP-TP FFN boundary (the default, headline line); the others measure "
-                         "the Delayed-TP stack, the attention-side boundary and the neuron permutation")
+                         "the Delayed-TP stack, the attention-side boundary, the neuron permutation and the "
+                         "boundary with E4M3 linear layers")
     return ap.parse_args()
 
 
@@ -541,6 +542,8 @@ def run_other(args):
                              "out_projection": {"ms": ms_o, "achieved": fo / (ms_o * 1e-3) / 1e12}},
                     roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                               "frac": value / pk["bf16_sustained"]})
+    elif args.workload == "fp8":
+        line.update(_fp8_line(args, synth.BOUNDARY_D4096, to_dev, dev, stream, pk))
     else:
         cfg = synth.DTP_STACK
         inp = synth.dtp_inputs(cfg)
@@ -564,6 +567,68 @@ def run_other(args):
                               "frac": gbs / pk["hbm"], "algorithmic_bytes": by})
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _fp8_line(args, cfg, to_dev, dev, stream, pk):
+    """The boundary with E4M3 linear layers on the 8192 x 4096 x 14336 P=2
+    workload: weights quantised once (timed apart: model state), then per
+    step prologue, quantise y, E4M3 gate/up + SwiGLU, quantise s, E4M3 down."""
+    import torch
+    import sequence_tensor_transformer_gb300 as st
+    from sequence_tensor_transformer_gb300 import synth
+
+    inp = synth.boundary_inputs(cfg)
+    T = {k: to_dev(v) for k, v in inp.items()}
+    M, d, F, P, f = cfg.M, cfg.d, cfg.F, cfg.P, cfg.F // cfg.P
+    qw = st.quantize_ffn_weights_e4m3(T["W1g"], T["W1u"], T["W2"], P)
+    ms_wq = timed(lambda: st.quantize_ffn_weights_e4m3(T["W1g"], T["W1u"], T["W2"], P), 20, 3, stream)
+    for k in ("W1g", "W1u", "W2"):
+        del T[k]
+    out = torch.empty((P, M, d), dtype=torch.bfloat16, device=dev)
+    h = torch.empty_like(T["x"])
+    ws = torch.empty(st.sptp_ffn_fp8_workspace_size(M, d, F, P, cfg.chunks), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: st.sptp_ffn_forward_fp8(T["x"], T["partials"], T["gamma"], qw, P, cfg.chunks, cfg.eps,
+                                               out=out, resid_out=h, workspace=ws), args.steps, args.warmup, stream)
+    assert st.sptp_read_device_status(ws) == 0
+    # the five launches of a step, each timed alone on the same buffers
+    hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
+    y = torch.empty_like(T["x"])
+    qy = torch.empty((M, d), dtype=torch.uint8, device=dev)
+    sy = torch.empty((M,), dtype=torch.float32, device=dev)
+    sb = torch.empty((P, M, f), dtype=torch.bfloat16, device=dev)
+    qs = torch.empty((P, M, f), dtype=torch.uint8, device=dev)
+    ss = torch.empty((P, M), dtype=torch.float32, device=dev)
+    n = max(20, args.steps // 5)
+    k = {}
+    k["prologue"] = timed(lambda: st.sptp_prologue(T["x"], T["partials"], T["gamma"], cfg.eps, h_out=h, y_out=y),
+                          n, 3, stream)
+    k["quantize_y"] = timed(lambda: st.sptp_quantize_rows_e4m3(y, q=qy, scale=sy), n, 3, stream)
+    k["gateup_e4m3"] = timed(lambda: st.sptp_gateup_swiglu_e4m3(qy, sy, qw[0], qw[1], qw[2], qw[3], P, s_out=sb,
+                                                                 workspace=hdr), n, 3, stream)
+    k["quantize_s"] = timed(lambda: st.sptp_quantize_rows_e4m3(sb, q=qs, scale=ss), n, 3, stream)
+    k["down_e4m3"] = timed(lambda: st.sptp_down_proj_e4m3(qs, ss, qw[4], qw[5], P, out=out, workspace=hdr), n, 3,
+                           stream)
+    fl_gu, fl_dn = 4.0 * M * d * F, 2.0 * M * d * F
+    # the kernel is timed alone in a short loop: the burst peak, times the
+    # nominal fp8 / bf16 dense ratio (4.5 / 2.25)
+    fp8_peak = 2.0 * pk["bf16_burst"]
+    value = 6.0 * M * d * F / (ms * 1e-3) / 1e12
+    kernels = {name: {"ms": t} for name, t in k.items()}
+    kernels["gateup_e4m3"]["achieved_tflops"] = fl_gu / (k["gateup_e4m3"] * 1e-3) / 1e12
+    kernels["down_e4m3"]["achieved_tflops"] = fl_dn / (k["down_e4m3"] * 1e-3) / 1e12
+    for name, R, K in (("quantize_y", M, d), ("quantize_s", P * M, f)):
+        kernels[name]["achieved_gbs"] = (3.0 * R * K + 4.0 * R) / (k[name] * 1e-3) / 1e9
+    gu = kernels["gateup_e4m3"]["achieved_tflops"]
+    return dict(metric="SP-TP FFN forward TFLOP/s with E4M3 linear layers (d=4096, M=8192)", value=value,
+                unit="TFLOP/s", ms_per_step=ms, tokens_per_s=M / (ms * 1e-3), dtype="e4m3",
+                config={"workload": cfg.name + "_e4m3", "M": M, "d": d, "F": F, "P": P, "chunks": cfg.chunks,
+                        "l2": "inputs larger than L2 (no flush)",
+                        "weights": "E4M3 + row scales, quantised once outside the timed region"},
+                weight_quantisation_ms=ms_wq, kernels=kernels,
+                roofline={"bound": "tensor", "kernel": "gateup_e4m3", "achieved": gu, "peak": fp8_peak,
+                          "unit": "TFLOP/s", "frac": gu / fp8_peak,
+                          "peak_note": "2 x measured burst bf16 (nominal fp8:bf16 dense ratio); the whole step "
+                                       "against 2 x sustained bf16: %.3f" % (value / (2.0 * pk["bf16_sustained"]))})
 
 
 def main():

@@ -204,6 +204,70 @@ int sptp_permute_ffn_neurons(const void* W1g, const void* W1u, const void* W2, c
                              void* W1g_out, void* W1u_out, void* W2_out,
                              void* workspace, size_t ws_bytes, void* cuda_stream);
 
+/* ---- fp8 (E4M3) linear layers ------------------------------------------------
+ * [A] "Additional Information" names fp8 (MXFP8) linear layers inside
+ * tensor-parallel blocks; the pages fix no scaling recipe.  This library's
+ * reading: every linear quantises its bf16 input row-wise (rows along the
+ * GEMM's reduction axis) to OCP E4M3 with a power-of-two scale, and its GEMM
+ * accumulates in fp32 on tcgen05 (kind::f8f6f4) and dequantises in the
+ * epilogue.  A power-of-two scale makes a * 2^-e exact, so the codes depend on
+ * the bf16 values alone.
+ */
+
+/*
+ * sptp_quantize_rows_e4m3 -- row-wise E4M3 quantisation of a bf16 [R][K]:
+ *     e_r      = least integer >= -126 with max_k |a[r][k]| <= 448 * 2^e_r
+ *     q[r][k]  = RNE_E4M3(a[r][k] * 2^-e_r)       (E4M3 bytes, [R][K])
+ *     scale[r] = 2^e_r                            (fp32, [R])
+ * The weights of sptp_ffn_forward_fp8 are quantised with it once: W1g and
+ * W1u as [F][d] (R = F, K = d: one scale per neuron) and W2 as [d*P][F/P]
+ * (R = d*P, K = F/P: one scale per output feature n and shard p, at index
+ * n*P + p -- shard p quantises its own slice).
+ *   R >= 0 (0 is a no-op), K > 0, K % 16 == 0; a and q 16-byte aligned,
+ *   scale 4-byte aligned; q and scale must not overlap a or each other.
+ *   Inputs must be finite (non-finite values are outside the contract).
+ */
+int sptp_quantize_rows_e4m3(const void* a, long long R, int K, void* q, float* scale,
+                            void* cuda_stream);
+
+/* Workspace bytes needed by sptp_ffn_forward_fp8 (0 on bad args).  Layout:
+ * header | y bf16 [M][d] | qy [M][d] | sy [M] | s bf16 [P][M][F/P] |
+ * qs [P][M][F/P] | ss [P][M], each part 256-byte aligned. */
+size_t sptp_ffn_fp8_workspace_size(int M, int d, int F, int P, int chunks);
+
+/*
+ * sptp_ffn_forward_fp8 -- sptp_ffn_forward with fp8 linear layers (bf16
+ * activations in and out).  Steps 1-3 as there (fp32 partial sum, residual
+ * add, RMSNorm); y is the bf16 activation; then for every shard p:
+ *     qy, sy = quantize_rows(y)                    (over d, one scale per token)
+ *     a      = (qy qW1g[F_p]^T) * sy[t] * sW1g[n]   b likewise with W1u
+ *     s_p    = bf16(silu(a) * b)
+ *     qs, ss = quantize_rows(s_p)                  (over F/P, per token and shard)
+ *     out[p] = bf16((qs qW2[:, F_p]^T) * ss[p][t] * sW2[n*P + p])
+ *   x, partials, gamma, out, resid_out, chunks, eps: as in sptp_ffn_forward
+ *   (bf16).  qW1g, qW1u [F][d] E4M3 with sW1g, sW1u [F] fp32; qW2 [d][F]
+ *   E4M3 with sW2 [d][P] fp32: the outputs of sptp_quantize_rows_e4m3 above.
+ *   Shape rules of sptp_ffn_forward plus d % 16 == 0 and (F/P) % 16 == 0.
+ */
+int sptp_ffn_forward_fp8(const void* x, const void* partials, const void* gamma,
+                         const void* qW1g, const float* sW1g, const void* qW1u, const float* sW1u,
+                         const void* qW2, const float* sW2,
+                         int M, int d, int F, int P, int chunks, float eps,
+                         void* out, void* resid_out,
+                         void* workspace, size_t ws_bytes, void* cuda_stream);
+
+/* The two fp8 GEMMs of sptp_ffn_forward_fp8 as separate launches:
+ *   sptp_gateup_swiglu_e4m3: s_out [P][M][F/P] bf16 from qy [M][d], sy [M].
+ *   sptp_down_proj_e4m3: out [P][M][d] bf16 from qs [P][M][F/P], ss [P][M].
+ * Weights and scales as in sptp_ffn_forward_fp8; workspace: at least
+ * SPTP_WS_HEADER_BYTES (status words). */
+int sptp_gateup_swiglu_e4m3(const void* qy, const float* sy, const void* qW1g, const float* sW1g,
+                            const void* qW1u, const float* sW1u, int M, int d, int F, int P,
+                            void* s_out, void* workspace, size_t ws_bytes, void* cuda_stream);
+int sptp_down_proj_e4m3(const void* qs, const float* ss, const void* qW2, const float* sW2,
+                        int M, int d, int F, int P, void* out,
+                        void* workspace, size_t ws_bytes, void* cuda_stream);
+
 /*
  * sptp_read_device_status -- synchronises `cuda_stream` and returns the
  * status the kernels recorded in the workspace header since the last call

@@ -18,7 +18,9 @@ __all__ = [
     "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
     "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "EXPORTED_SYMBOLS",
     "sptp_ffn_forward_noalloc", "SPTP_NOALLOC_SCRATCH_BYTES", "sptp_permute_ffn_neurons",
-    "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward",
+    "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward", "sptp_quantize_rows_e4m3",
+    "quantize_ffn_weights_e4m3", "sptp_ffn_fp8_workspace_size", "sptp_ffn_forward_fp8",
+    "sptp_gateup_swiglu_e4m3", "sptp_down_proj_e4m3",
 ]
 
 SPTP_BF16 = 0
@@ -32,11 +34,14 @@ EXPORTED_SYMBOLS = (
     "dtp_ffn_stack_forward", "sptp_prologue", "sptp_gateup_swiglu", "sptp_down_proj",
     "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "sptp_ffn_forward_noalloc",
     "sptp_permute_ffn_neurons", "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward",
+    "sptp_quantize_rows_e4m3", "sptp_ffn_fp8_workspace_size", "sptp_ffn_forward_fp8", "sptp_gateup_swiglu_e4m3",
+    "sptp_down_proj_e4m3",
 )
 
 _lib = None
 
 _P, _I, _F, _Z, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_ulonglong
+_LL = ctypes.c_longlong
 _SIGS = {
     "sptp_ffn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "sptp_ffn_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _Z, _P]),
@@ -52,6 +57,12 @@ _SIGS = {
     "sptp_permute_ffn_neurons": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "sptp_attn_qkv_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I]),
     "sptp_attn_qkv_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _Z, _P]),
+    "sptp_quantize_rows_e4m3": (_I, [_P, _LL, _I, _P, _P, _P]),
+    "sptp_ffn_fp8_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "sptp_ffn_forward_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, _P, _Z,
+                                  _P]),
+    "sptp_gateup_swiglu_e4m3": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "sptp_down_proj_e4m3": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
 }
 
 
@@ -261,3 +272,83 @@ def sptp_read_device_status(workspace, stream=None) -> int:
 def sptp_wait_selftest(workspace, limit_ns: int, preset_flag: bool, stream=None) -> int:
     return int(lib().sptp_wait_selftest(_ptr(workspace), workspace.numel(), int(limit_ns), int(preset_flag),
                                         _stream(stream)))
+
+
+# ------------------------------------------------------------------ fp8 (E4M3)
+
+def sptp_quantize_rows_e4m3(a, q=None, scale=None, stream=None):
+    """Row-wise E4M3 quantisation of a bf16 tensor viewed as [R][K] (K = the
+    last dimension).  Returns (q uint8 [..., K], scale float32 [...]):
+    a ~= q * scale[..., None] with scale a power of two per row."""
+    if a.dtype != torch.bfloat16:
+        raise TypeError("bf16 input expected")
+    K = a.shape[-1]
+    R = a.numel() // K if K else 0
+    if q is None:
+        q = torch.empty(a.shape, dtype=torch.uint8, device=a.device)
+    if scale is None:
+        scale = torch.empty(a.shape[:-1], dtype=torch.float32, device=a.device)
+    code = lib().sptp_quantize_rows_e4m3(_ptr(a), R, K, _ptr(q), _ptr(scale), _stream(stream))
+    _check("sptp_quantize_rows_e4m3", code)
+    return q, scale
+
+
+def quantize_ffn_weights_e4m3(W1g, W1u, W2, P, stream=None):
+    """The fp8 weights of one FFN in the layout sptp_ffn_forward_fp8 takes:
+    (qW1g, sW1g [F], qW1u, sW1u [F], qW2 [d,F], sW2 [d,P]); W2 is quantised as
+    [d*P][F/P] rows, one scale per output feature and shard."""
+    d, F = W2.shape
+    qg, sg = sptp_quantize_rows_e4m3(W1g, stream=stream)
+    qu, su = sptp_quantize_rows_e4m3(W1u, stream=stream)
+    q2, s2 = sptp_quantize_rows_e4m3(W2.view(d, P, F // P), stream=stream)
+    return qg, sg, qu, su, q2.view(d, F), s2
+
+
+def sptp_ffn_fp8_workspace_size(M, d, F, P, chunks) -> int:
+    return int(lib().sptp_ffn_fp8_workspace_size(M, d, F, P, chunks))
+
+
+def sptp_ffn_forward_fp8(x, partials, gamma, qweights, P, chunks, eps, out=None, resid_out=None, workspace=None,
+                         stream=None, write_resid=True):
+    """SP-TP FFN boundary with E4M3 linear layers; qweights as returned by
+    quantize_ffn_weights_e4m3.  Returns (out [P,M,d], resid_out [M,d] or None)."""
+    qg, sg, qu, su, q2, s2 = qweights
+    M, d = x.shape
+    F = qg.shape[0]
+    if out is None:
+        out = torch.empty((P, M, d), dtype=x.dtype, device=x.device)
+    if resid_out is None and write_resid:
+        resid_out = torch.empty_like(x)
+    if workspace is None:
+        workspace = _workspace(sptp_ffn_fp8_workspace_size(M, d, F, P, chunks), x.device)
+    code = lib().sptp_ffn_forward_fp8(
+        _ptr(x), _ptr(partials), _ptr(gamma), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(q2), _ptr(s2), M, d, F,
+        P, chunks, float(eps), _ptr(out), _ptr(resid_out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("sptp_ffn_forward_fp8", code)
+    return out, resid_out
+
+
+def sptp_gateup_swiglu_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, P, s_out=None, workspace=None, stream=None):
+    M, d = qy.shape
+    F = qW1g.shape[0]
+    if s_out is None:
+        s_out = torch.empty((P, M, F // P), dtype=torch.bfloat16, device=qy.device)
+    if workspace is None:
+        workspace = _workspace(SPTP_WS_HEADER_BYTES, qy.device)
+    code = lib().sptp_gateup_swiglu_e4m3(_ptr(qy), _ptr(sy), _ptr(qW1g), _ptr(sW1g), _ptr(qW1u), _ptr(sW1u), M, d,
+                                         F, P, _ptr(s_out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("sptp_gateup_swiglu_e4m3", code)
+    return s_out
+
+
+def sptp_down_proj_e4m3(qs, ss, qW2, sW2, P, out=None, workspace=None, stream=None):
+    _, M, f = qs.shape
+    d, F = qW2.shape
+    if out is None:
+        out = torch.empty((P, M, d), dtype=torch.bfloat16, device=qs.device)
+    if workspace is None:
+        workspace = _workspace(SPTP_WS_HEADER_BYTES, qs.device)
+    code = lib().sptp_down_proj_e4m3(_ptr(qs), _ptr(ss), _ptr(qW2), _ptr(sW2), M, d, F, P, _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("sptp_down_proj_e4m3", code)
+    return out

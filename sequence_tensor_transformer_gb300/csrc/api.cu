@@ -316,6 +316,100 @@ int band_for_chunks(int M, int chunks) {
 constexpr int SPTP_ERR_UNSUPPORTED = -100;  // internal: fused path not available here
 constexpr int kFirstBandRows = 2048;
 
+// ------------------------------------------------------------ fp8 (E4M3)
+
+constexpr int kBK8 = 128;  // E4M3 elements per 128-byte swizzle row
+
+int check_fp8(int M, int d, int F, int P) {
+    const int rc = check_common(M, d, F, P, SPTP_BF16);
+    if (rc != SPTP_OK) return rc;
+    if (d % 16 != 0 || (F / P) % 16 != 0) return SPTP_ERR_SHAPE;
+    return SPTP_OK;
+}
+
+// E4M3 gate/up + SwiGLU for P groups on the CTA-pair tcgen05 GEMM.
+int gateup_e4m3(const void* qy, const float* sy, const void* qW1g, const float* sW1g, const void* qW1u,
+                const float* sW1u, int M, int d, int F, int P, void* s_out, DeviceStatus* st, int band,
+                const DevInfo& di, cudaStream_t s) {
+    const int f = F / P;
+    if (M == 0) return SPTP_OK;
+    TcGemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int g = 0; g < P; ++g) {
+        const size_t woff = static_cast<size_t>(g) * f * d;
+        if (!encode_map_u8(&p.mapA[g], qy, d, M, d, kBK8, kBM) ||
+            !encode_map_u8(&p.mapB0[g], cptr(qW1g, woff), d, f, d, kBK8, kBNSwiGLU) ||
+            !encode_map_u8(&p.mapB1[g], cptr(qW1u, woff), d, f, d, kBK8, kBNSwiGLU))
+            return SPTP_ERR_CUDA;
+        p.out[g] = mptr(s_out, static_cast<size_t>(g) * M * f * 2);
+        p.row_scale[g] = sy;
+        p.col_scale0[g] = sW1g + static_cast<size_t>(g) * f;
+        p.col_scale1[g] = sW1u + static_cast<size_t>(g) * f;
+    }
+    p.col_scale_stride = 1;
+    p.ldo = f;
+    p.M = M;
+    p.N = f;
+    p.K = d;
+    p.G = P;
+    p.mt = (M + 2 * kBM - 1) / (2 * kBM);
+    p.nt = (f + kBNSwiGLU - 1) / kBNSwiGLU;
+    p.nk = (d + kBK8 - 1) / kBK8;
+    band = (band + 1) / 2;
+    p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
+    p.status = st;
+    p.wait_limit_ns = kWaitLimitNs;
+    return cuda_status(launch_tc_gemm_pair_e4m3(p, Epi::kSwiGLU, di.sms, s));
+}
+
+// E4M3 down projection for P groups: out_g = (qs_g qW2[:, F_g]^T) ss_g sW2[:, g].
+int down_e4m3(const void* qs, const float* ss, const void* qW2, const float* sW2, int M, int d, int F, int P,
+              void* const* out, DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
+    const int f = F / P;
+    if (M == 0) return SPTP_OK;
+    TcGemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int g = 0; g < P; ++g) {
+        if (!encode_map_u8(&p.mapA[g], cptr(qs, static_cast<size_t>(g) * M * f), f, M, f, kBK8, kBM) ||
+            !encode_map_u8(&p.mapB0[g], cptr(qW2, static_cast<size_t>(g) * f), f, d, F, kBK8, kBNStore / 2))
+            return SPTP_ERR_CUDA;
+        p.out[g] = out[g];
+        p.row_scale[g] = ss + static_cast<size_t>(g) * M;
+        p.col_scale0[g] = sW2 + g;
+    }
+    p.col_scale_stride = P;
+    p.ldo = d;
+    p.M = M;
+    p.N = d;
+    p.K = f;
+    p.G = P;
+    p.mt = (M + 2 * kBM - 1) / (2 * kBM);
+    p.nt = (d + kBNStore - 1) / kBNStore;
+    p.nk = (f + kBK8 - 1) / kBK8;
+    band = (band + 1) / 2;
+    p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
+    p.status = st;
+    p.wait_limit_ns = kWaitLimitNs;
+    return cuda_status(launch_tc_gemm_pair_e4m3(p, Epi::kStore, di.sms, s));
+}
+
+struct Fp8Layout {
+    size_t y, qy, sy, s, qs, ss, total;
+};
+
+Fp8Layout fp8_layout(int M, int d, int F, int P) {
+    Fp8Layout L;
+    const size_t md = static_cast<size_t>(M) * d, mf = static_cast<size_t>(M) * F;
+    L.y = SPTP_WS_HEADER_BYTES;
+    L.qy = L.y + align_up(md * 2);
+    L.sy = L.qy + align_up(md);
+    L.s = L.sy + align_up(static_cast<size_t>(M) * 4);
+    L.qs = L.s + align_up(mf * 2);
+    L.ss = L.qs + align_up(mf);
+    L.total = L.ss + align_up(static_cast<size_t>(M) * P * 4);
+    return L;
+}
+
 // The whole bf16 boundary as one persistent launch (fused.cu).  Returns
 // SPTP_ERR_UNSUPPORTED, having enqueued nothing, where it cannot launch.
 int fused_forward(const void* x, const void* partials, const void* gamma, const void* W1g, const void* W1u,
@@ -894,6 +988,152 @@ int sptp_wait_selftest(void* workspace, size_t ws_bytes, unsigned long long limi
             return SPTP_ERR_CUDA;
     }
     return cuda_status(launch_wait_selftest(ws_status(workspace), limit_ns, s));
+}
+
+int sptp_quantize_rows_e4m3(const void* a, long long R, int K, void* q, float* scale, void* cuda_stream) {
+    if (R < 0 || K <= 0 || K % 16 != 0 || R > (1ll << 40) / K) return SPTP_ERR_SHAPE;
+    if (R == 0) return SPTP_OK;
+    if (!a || !q || !scale) return SPTP_ERR_NULL;
+    if (!aligned16(a) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0) return SPTP_ERR_SHAPE;
+    const size_t ab = static_cast<size_t>(R) * K * 2, qb = static_cast<size_t>(R) * K, sb = static_cast<size_t>(R) * 4;
+    if (overlaps(q, qb, a, ab) || overlaps(scale, sb, a, ab) || overlaps(scale, sb, q, qb)) return SPTP_ERR_ALIAS;
+    DevInfo di;
+    const int rc = device_info(&di);
+    if (rc != SPTP_OK) return rc;
+    return cuda_status(launch_quantize_rows_e4m3(a, R, K, q, scale, di.sms, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+size_t sptp_ffn_fp8_workspace_size(int M, int d, int F, int P, int chunks) {
+    if (check_fp8(M, d, F, P) != SPTP_OK || chunks < 1) return 0;
+    return fp8_layout(M, d, F, P).total;
+}
+
+int sptp_ffn_forward_fp8(const void* x, const void* partials, const void* gamma, const void* qW1g, const float* sW1g,
+                         const void* qW1u, const float* sW1u, const void* qW2, const float* sW2, int M, int d, int F,
+                         int P, int chunks, float eps, void* out, void* resid_out, void* workspace, size_t ws_bytes,
+                         void* cuda_stream) {
+    if (!gamma || !qW1g || !sW1g || !qW1u || !sW1u || !qW2 || !sW2 || !workspace ||
+        (M != 0 && (!x || !partials || !out)))
+        return SPTP_ERR_NULL;
+    int rc = check_fp8(M, d, F, P);
+    if (rc != SPTP_OK) return rc;
+    if (chunks < 1 || chunks % P != 0 || (M > 0 && M % chunks != 0)) return SPTP_ERR_SHAPE;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
+    const void* ptrs[] = {x, partials, gamma, qW1g, qW1u, qW2, out, resid_out, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    const void* sc[] = {sW1g, sW1u, sW2};
+    for (const void* q : sc)
+        if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return SPTP_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return SPTP_ERR_SHAPE;
+    const Fp8Layout lay = fp8_layout(M, d, F, P);
+    if (ws_bytes < lay.total) return SPTP_ERR_WORKSPACE;
+    const size_t act = static_cast<size_t>(M) * d * 2;
+    const size_t out_bytes = act * P;
+    const size_t wq = static_cast<size_t>(F) * d;
+    const void* ins[] = {x, partials, gamma, qW1g, sW1g, qW1u, sW1u, qW2, sW2, workspace, resid_out};
+    const size_t insz[] = {act, out_bytes, static_cast<size_t>(d) * 2, wq, static_cast<size_t>(F) * 4, wq,
+                           static_cast<size_t>(F) * 4, wq, static_cast<size_t>(d) * P * 4, lay.total,
+                           resid_out ? act : 0};
+    for (int i = 0; i < 11; ++i)
+        if (overlaps(out, out_bytes, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    for (int i = 0; i < 9; ++i)
+        if (overlaps(workspace, lay.total, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    if (resid_out && resid_out != x) {
+        for (int i = 0; i < 10; ++i)
+            if (i != 0 && overlaps(resid_out, act, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+        if (overlaps(resid_out, act, x, act)) return SPTP_ERR_ALIAS;
+    }
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    DeviceStatus* st = ws_status(workspace);
+    void* y = mptr(workspace, lay.y);
+    void* qy = mptr(workspace, lay.qy);
+    float* sy = reinterpret_cast<float*>(mptr(workspace, lay.sy));
+    void* sbuf = mptr(workspace, lay.s);
+    void* qs = mptr(workspace, lay.qs);
+    float* ss = reinterpret_cast<float*>(mptr(workspace, lay.ss));
+    const int band = band_for_chunks(M, chunks);
+    const int f = F / P;
+
+    // 1-3: partial sum, residual add, RMSNorm -> the bf16 activation y
+    PrologueParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.G = 1;
+    pp.M = M;
+    pp.d = d;
+    pp.eps = eps;
+    pp.gamma = gamma;
+    pp.grp[0] = PrologueGroup{x, resid_out, y, 0, P};
+    for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
+    pp.status = st;
+    pp.wait_limit_ns = kWaitLimitNs;
+    if ((rc = cuda_status(launch_prologue(pp, true, di.sms, s))) != SPTP_OK) return rc;
+    // the gate/up linear quantises its input per token
+    if ((rc = cuda_status(launch_quantize_rows_e4m3(y, M, d, qy, sy, di.sms, s))) != SPTP_OK) return rc;
+    // 4-6: (identity) gather + column-parallel E4M3 gate/up + SwiGLU
+    if ((rc = gateup_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, M, d, F, P, sbuf, st, band, di, s)) != SPTP_OK) return rc;
+    // the down linear quantises s per token within each shard
+    if ((rc = cuda_status(launch_quantize_rows_e4m3(sbuf, static_cast<long long>(P) * M, f, qs, ss, di.sms, s))) !=
+        SPTP_OK)
+        return rc;
+    // 7: row-parallel E4M3 down projection, one partial per shard
+    void* outs[kMaxGroups];
+    for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * act);
+    return down_e4m3(qs, ss, qW2, sW2, M, d, F, P, outs, st, band, di, s);
+}
+
+int sptp_gateup_swiglu_e4m3(const void* qy, const float* sy, const void* qW1g, const float* sW1g, const void* qW1u,
+                            const float* sW1u, int M, int d, int F, int P, void* s_out, void* workspace,
+                            size_t ws_bytes, void* cuda_stream) {
+    if (!qW1g || !sW1g || !qW1u || !sW1u || !workspace || (M != 0 && (!qy || !sy || !s_out))) return SPTP_ERR_NULL;
+    int rc = check_fp8(M, d, F, P);
+    if (rc != SPTP_OK) return rc;
+    const void* ptrs[] = {qy, sy, qW1g, sW1g, qW1u, sW1u, s_out, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    if (ws_bytes < SPTP_WS_HEADER_BYTES) return SPTP_ERR_WORKSPACE;
+    const size_t sb = static_cast<size_t>(M) * F * 2, wq = static_cast<size_t>(F) * d;
+    const void* ins[] = {qy, sy, qW1g, sW1g, qW1u, sW1u, workspace};
+    const size_t insz[] = {static_cast<size_t>(M) * d, static_cast<size_t>(M) * 4, wq, static_cast<size_t>(F) * 4,
+                           wq, static_cast<size_t>(F) * 4, SPTP_WS_HEADER_BYTES};
+    for (int i = 0; i < 7; ++i)
+        if (overlaps(s_out, sb, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    return gateup_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, M, d, F, P, s_out, ws_status(workspace),
+                       band_for_chunks(M, 1), di, s);
+}
+
+int sptp_down_proj_e4m3(const void* qs, const float* ss, const void* qW2, const float* sW2, int M, int d, int F,
+                        int P, void* out, void* workspace, size_t ws_bytes, void* cuda_stream) {
+    if (!qW2 || !sW2 || !workspace || (M != 0 && (!qs || !ss || !out))) return SPTP_ERR_NULL;
+    int rc = check_fp8(M, d, F, P);
+    if (rc != SPTP_OK) return rc;
+    const void* ptrs[] = {qs, ss, qW2, sW2, out, workspace};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    if (ws_bytes < SPTP_WS_HEADER_BYTES) return SPTP_ERR_WORKSPACE;
+    const size_t ob = static_cast<size_t>(P) * M * d * 2;
+    const void* ins[] = {qs, ss, qW2, sW2, workspace};
+    const size_t insz[] = {static_cast<size_t>(M) * F, static_cast<size_t>(M) * P * 4, static_cast<size_t>(F) * d,
+                           static_cast<size_t>(d) * P * 4, SPTP_WS_HEADER_BYTES};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(out, ob, ins[i], insz[i])) return SPTP_ERR_ALIAS;
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
+    void* outs[kMaxGroups];
+    for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * M * d * 2);
+    return down_e4m3(qs, ss, qW2, sW2, M, d, F, P, outs, ws_status(workspace), band_for_chunks(M, 1), di, s);
 }
 
 }  // extern "C"

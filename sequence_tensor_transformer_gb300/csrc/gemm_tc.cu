@@ -282,11 +282,43 @@ constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
 constexpr int B_BYTES = 128 * BK * 2;        // 16 KiB (half of the B tile)
 constexpr int PSTAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + BAR_BYTES;
-constexpr uint32_t PIDESC = idesc_bf16_f32(PBM, PBN);
+// A stage holds 128-byte K slices of each operand row: 64 bf16 or 128 E4M3
+// elements.  Either way 4 UMMAs of 32 bytes per row consume it.
+template <bool E4M3>
+constexpr int k_elems() { return E4M3 ? 128 : 64; }
+template <bool E4M3>
+constexpr uint32_t pair_idesc() { return E4M3 ? idesc_e4m3_f32(PBM, PBN) : idesc_bf16_f32(PBM, PBN); }
 // Epilogue warps EW: 4 (one per TMEM lane quarter) or 8 (two per quarter,
 // each taking half of the tile's columns).
 template <int EW>
 constexpr int pair_threads() { return 32 * (2 + EW); }
+
+// Column scales of 32 consecutive output columns from col; columns past N
+// read none (their products are discarded).  Every lane reads the same
+// addresses: one broadcast transaction per load.
+__device__ __forceinline__ void load_col_scales(const float* sg, const float* su, int col, int N, float* cg,
+                                                float* cu) {
+    if (col + 32 <= N) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(sg + col) + v);
+            const float4 b = __ldg(reinterpret_cast<const float4*>(su + col) + v);
+            cg[4 * v] = a.x, cg[4 * v + 1] = a.y, cg[4 * v + 2] = a.z, cg[4 * v + 3] = a.w;
+            cu[4 * v] = b.x, cu[4 * v + 1] = b.y, cu[4 * v + 2] = b.z, cu[4 * v + 3] = b.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            cg[j] = col + j < N ? __ldg(sg + col + j) : 0.0f;
+            cu[j] = col + j < N ? __ldg(su + col + j) : 0.0f;
+        }
+    }
+}
+
+__device__ __forceinline__ void load_col_scales_strided(const float* sc, int stride, int col, int N, float* cs) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cs[j] = col + j < N ? __ldg(sc + static_cast<long long>(col + j) * stride) : 0.0f;
+}
 
 struct Bars {
     uint64_t full[PSTAGES];
@@ -299,8 +331,9 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block too large");
 
-template <Epi EPI, int EW>
+template <Epi EPI, int EW, bool E4M3>
 __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
+    constexpr int KE = k_elems<E4M3>();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -369,13 +402,13 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                     armed_parity[stage] = static_cast<int>(phase);
                 }
                 const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
-                tma_load_2d_pair(a_tiles + stage * A_BYTES, &p.mapA[g], fb, kb * BK,
+                tma_load_2d_pair(a_tiles + stage * A_BYTES, &p.mapA[g], fb, kb * KE,
                                  m * PBM + static_cast<int>(rank) * 128);
                 uint8_t* bt = b_tiles + stage * B_BYTES;
                 if (EPI == Epi::kSwiGLU) {
-                    tma_load_2d_pair(bt, rank == 0 ? &p.mapB0[g] : &p.mapB1[g], fb, kb * BK, n * 128);
+                    tma_load_2d_pair(bt, rank == 0 ? &p.mapB0[g] : &p.mapB1[g], fb, kb * KE, n * 128);
                 } else {
-                    tma_load_2d_pair(bt, &p.mapB0[g], fb, kb * BK, n * PBN + static_cast<int>(rank) * 128);
+                    tma_load_2d_pair(bt, &p.mapB0[g], fb, kb * KE, n * PBN + static_cast<int>(rank) * 128);
                 }
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -417,8 +450,14 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                 const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(a_tiles + stage * A_BYTES));
                 const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(b_tiles + stage * B_BYTES));
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, PIDESC, (kb | k) != 0 ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) {
+                    if constexpr (E4M3)
+                        umma_e4m3_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, pair_idesc<E4M3>(),
+                                       (kb | k) != 0 ? 1u : 0u);
+                    else
+                        umma_bf16_pair(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, pair_idesc<E4M3>(),
+                                       (kb | k) != 0 ? 1u : 0u);
+                }
                 umma_commit_pair_multicast(&bars->empty[stage], 0x3);
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -456,21 +495,32 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[g]) + static_cast<long long>(row) * p.ldo;
+            // E4M3: the token row's scale (power of two; rows past M read none)
+            float rs = 1.0f;
+            if constexpr (E4M3) rs = row_ok ? __ldg(p.row_scale[g] + row) : 0.0f;
             if (EPI == Epi::kSwiGLU) {
 #pragma unroll 1
                 for (int c = half * (PBN / 2 / kSplits); c < (half + 1) * (PBN / 2 / kSplits); c += 32) {
                     uint32_t gv[32], uv[32];
                     tmem_ld_32cols(taddr + c, gv);
                     tmem_ld_32cols(taddr + PBN / 2 + c, uv);
+                    const int col = n * (PBN / 2) + c;
+                    float cg[32], cu[32];
+                    if constexpr (E4M3) load_col_scales(p.col_scale0[g], p.col_scale1[g], col, p.N, cg, cu);
                     tmem_ld_wait();
                     uint32_t packed[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
-                        const float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
+                        float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
+                        float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
+                        if constexpr (E4M3) {
+                            a0 = a0 * rs * cg[2 * j];
+                            a1 = a1 * rs * cg[2 * j + 1];
+                            b0 = b0 * rs * cu[2 * j];
+                            b1 = b1 * rs * cu[2 * j + 1];
+                        }
                         packed[j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
                     }
-                    const int col = n * (PBN / 2) + c;
                     if (row_ok) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
@@ -484,12 +534,20 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                 for (int c = half * (PBN / kSplits); c < (half + 1) * (PBN / kSplits); c += 32) {
                     uint32_t v32[32];
                     tmem_ld_32cols(taddr + c, v32);
+                    const int col = n * PBN + c;
+                    float cs[32];
+                    if constexpr (E4M3) load_col_scales_strided(p.col_scale0[g], p.col_scale_stride, col, p.N, cs);
                     tmem_ld_wait();
                     uint32_t packed[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        packed[j] = pack_bf16x2(__uint_as_float(v32[2 * j]), __uint_as_float(v32[2 * j + 1]));
-                    const int col = n * PBN + c;
+                    for (int j = 0; j < 16; ++j) {
+                        float v0 = __uint_as_float(v32[2 * j]), v1 = __uint_as_float(v32[2 * j + 1]);
+                        if constexpr (E4M3) {
+                            v0 = v0 * rs * cs[2 * j];
+                            v1 = v1 * rs * cs[2 * j + 1];
+                        }
+                        packed[j] = pack_bf16x2(v0, v1);
+                    }
                     if (row_ok) {
                         // the partials are final outputs: evict-first stores
 #pragma unroll
@@ -545,6 +603,20 @@ bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool encode_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                   uint32_t box_inner, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = get_encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_map_bf16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                         const uint64_t* strides_bytes, const uint32_t* box) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = get_encode_fn();
@@ -584,9 +656,9 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStre
 
 namespace {
 
-template <Epi EPI, int EW>
+template <Epi EPI, int EW, bool E4M3 = false>
 cudaError_t launch_pair_typed(const TcGemmParams& p, int num_sms, cudaStream_t s) {
-    auto* kfn = pair::tc_gemm_pair_kernel<EPI, EW>;
+    auto* kfn = pair::tc_gemm_pair_kernel<EPI, EW, E4M3>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::PSMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -629,6 +701,12 @@ cudaError_t launch_tc_gemm_pair(const TcGemmParams& p, Epi epi, int num_sms, cud
     // vs 1209, per-module Delayed-TP stack 856 vs 825).
     return epi == Epi::kSwiGLU ? launch_pair_typed<Epi::kSwiGLU, 4>(p, num_sms, s)
                                : launch_pair_typed<Epi::kStore, 4>(p, num_sms, s);
+}
+
+cudaError_t launch_tc_gemm_pair_e4m3(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s) {
+    if (p.G * p.mt * p.nt == 0) return cudaSuccess;
+    return epi == Epi::kSwiGLU ? launch_pair_typed<Epi::kSwiGLU, 4, true>(p, num_sms, s)
+                               : launch_pair_typed<Epi::kStore, 4, true>(p, num_sms, s);
 }
 
 }  // namespace sptp

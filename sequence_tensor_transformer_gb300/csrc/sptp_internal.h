@@ -79,6 +79,12 @@ struct TcGemmParams {
     int band;              // m-tiles per raster band
     DeviceStatus* status;
     unsigned long long wait_limit_ns;
+    // E4M3 operands only: power-of-two dequantisation scales, applied in the
+    // epilogue as acc * row_scale[row] * col_scale[col * col_scale_stride]
+    const float* row_scale[kMaxGroups];   // per A row (token)
+    const float* col_scale0[kMaxGroups];  // per output column (B0 row)
+    const float* col_scale1[kMaxGroups];  // per SwiGLU up column (B1 row)
+    int col_scale_stride;
 };
 
 enum class Epi { kSwiGLU, kStore };
@@ -87,7 +93,20 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStre
 // CTA-pair (cta_group::2) variant: tiles of 256 rows (mt counts 256-row tiles)
 // and 256 B rows; same parameter block and tensor maps (boxes of 128 rows).
 cudaError_t launch_tc_gemm_pair(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
+// The same CTA-pair GEMM on E4M3 operands (tcgen05 kind::f8f6f4; tensor maps
+// of bytes with boxes of 128 x 128), dequantised in the epilogue.
+cudaError_t launch_tc_gemm_pair_e4m3(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
 size_t tc_gemm_smem_bytes();
+
+// Encodes a 2-D byte (E4M3) tensor map with 128-byte swizzle.
+bool encode_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                   uint32_t box_inner, uint32_t box_outer);
+
+// Row-wise E4M3 quantiser: q[r][k] = RNE_E4M3(a[r][k] * 2^-e_r), scale[r] =
+// 2^e_r with e_r the least integer >= -126 such that max_k |a[r][k]| <=
+// 448 * 2^e_r.  a bf16 [R][K], K % 8 == 0.
+cudaError_t launch_quantize_rows_e4m3(const void* a, long long R, int K, void* q, float* scale, int num_sms,
+                                      cudaStream_t s);
 
 // Encodes a 2-D bf16 tensor map (inner = contiguous dim) with 128-byte swizzle.
 bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

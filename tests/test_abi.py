@@ -100,3 +100,34 @@ def test_step_entry_points_reject_bad_arguments(lib):
                                   None) == -2
     assert lib.sptp_down_proj(FAKE, FAKE * 2, 64, 128, 512, 2, 0, FAKE * 3, FAKE * 4, 100, None) == -4
     assert lib.sptp_wait_selftest(FAKE, 100, 1000, 0, None) == -4
+
+
+def test_fp8_entry_points_reject_bad_arguments(lib):
+    SHAPE, NULL, WS, ALIAS = -2, -1, -4, -8
+    q = lambda a=FAKE, R=64, K=128, qq=FAKE * 4096, sc=FAKE * 8192: lib.sptp_quantize_rows_e4m3(a, R, K, qq, sc, None)
+    assert q(R=0) == 0                 # empty: a no-op before any CUDA call
+    assert q(K=136) == SHAPE           # K % 16
+    assert q(K=0) == SHAPE
+    assert q(R=-1) == SHAPE
+    assert q(a=None) == NULL
+    assert q(a=FAKE + 8) == SHAPE      # misaligned
+    assert q(qq=FAKE + 64) == ALIAS    # codes overlap the input
+    assert q(sc=FAKE * 4096 + 64) == ALIAS
+
+    def f8(M=64, d=128, F=512, P=2, C=4, ptrs=None, out=FAKE * 64 * 4096, ws=FAKE * 128 * 4096,
+           ws_bytes=1 << 40):
+        p = ptrs or [FAKE * (i + 1) * 4096 for i in range(9)]
+        return lib.sptp_ffn_forward_fp8(*p, M, d, F, P, C, 1e-6, out, None, ws, ws_bytes, None)
+    assert f8(d=136) == SHAPE          # d % 16 (TMA rows of E4M3 bytes)
+    assert f8(F=2 * 24) == SHAPE       # F/P % 16
+    assert f8(C=3) == SHAPE
+    assert f8(ws_bytes=100) == WS
+    assert f8(ptrs=[None] + [FAKE * 4096] * 8) == NULL
+    assert f8(out=FAKE * 3 * 4096) == ALIAS   # out on top of gamma
+    n = st.sptp_ffn_fp8_workspace_size(64, 128, 512, 2, 4)
+    assert n >= 4096 + 64 * 128 * 3 + 64 * 4 + 64 * 512 * 3 + 2 * 64 * 4
+    assert st.sptp_ffn_fp8_workspace_size(64, 136, 512, 2, 4) == 0
+    assert lib.sptp_gateup_swiglu_e4m3(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 64, 128, 2 * 24, 2,
+                                       FAKE * 7, FAKE * 8, 1 << 20, None) == SHAPE
+    assert lib.sptp_down_proj_e4m3(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 64, 128, 512, 2, FAKE * 5, FAKE * 6, 100,
+                                   None) == WS
