@@ -256,6 +256,18 @@ int sptp_ffn_forward_fp8(const void* x, const void* partials, const void* gamma,
                          void* out, void* resid_out,
                          void* workspace, size_t ws_bytes, void* cuda_stream);
 
+/*
+ * sptp_prologue_e4m3 -- steps 1-3 with the gate/up linear's quantisation of y
+ * fused (one launch where a row's sources fit the kernel's shared-memory
+ * ring; otherwise y is stored to y_work and quantised by a second launch):
+ * h = x + sum_p partials[p]; y = bf16(RMSNorm(h) * gamma); q_out [M][d] and
+ * scale_out [M] as sptp_quantize_rows_e4m3(y).  bf16 only; h_out may be NULL
+ * or x; y_work [M][d] bf16 scratch (contents undefined afterwards); d % 16 == 0.
+ */
+int sptp_prologue_e4m3(const void* x, const void* partials, const void* gamma,
+                       int M, int d, int P, float eps,
+                       void* h_out, void* y_work, void* q_out, float* scale_out, void* cuda_stream);
+
 /* The two fp8 GEMMs of sptp_ffn_forward_fp8 as separate launches:
  *   sptp_gateup_swiglu_e4m3: s_out [P][M][F/P] bf16 from qy [M][d], sy [M].
  *   sptp_down_proj_e4m3: out [P][M][d] bf16 from qs [P][M][F/P], ss [P][M].

@@ -20,7 +20,7 @@ __all__ = [
     "sptp_ffn_forward_noalloc", "SPTP_NOALLOC_SCRATCH_BYTES", "sptp_permute_ffn_neurons",
     "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward", "sptp_quantize_rows_e4m3",
     "quantize_ffn_weights_e4m3", "sptp_ffn_fp8_workspace_size", "sptp_ffn_forward_fp8",
-    "sptp_gateup_swiglu_e4m3", "sptp_down_proj_e4m3",
+    "sptp_gateup_swiglu_e4m3", "sptp_down_proj_e4m3", "sptp_prologue_e4m3",
 ]
 
 SPTP_BF16 = 0
@@ -35,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "sptp_ffn_forward_noalloc",
     "sptp_permute_ffn_neurons", "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward",
     "sptp_quantize_rows_e4m3", "sptp_ffn_fp8_workspace_size", "sptp_ffn_forward_fp8", "sptp_gateup_swiglu_e4m3",
-    "sptp_down_proj_e4m3",
+    "sptp_down_proj_e4m3", "sptp_prologue_e4m3",
 )
 
 _lib = None
@@ -63,6 +63,7 @@ _SIGS = {
                                   _P]),
     "sptp_gateup_swiglu_e4m3": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "sptp_down_proj_e4m3": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "sptp_prologue_e4m3": (_I, [_P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
 }
 
 
@@ -326,6 +327,26 @@ def sptp_ffn_forward_fp8(x, partials, gamma, qweights, P, chunks, eps, out=None,
         P, chunks, float(eps), _ptr(out), _ptr(resid_out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("sptp_ffn_forward_fp8", code)
     return out, resid_out
+
+
+def sptp_prologue_e4m3(x, partials, gamma, eps, h_out=None, y_work=None, q_out=None, scale_out=None, stream=None,
+                       write_h=True):
+    """Partial sum + residual + RMSNorm with y quantised to E4M3 in the same
+    launch.  Returns (h or None, q uint8 [M,d], scale float32 [M])."""
+    M, d = x.shape
+    P = partials.shape[0]
+    if h_out is None and write_h:
+        h_out = torch.empty_like(x)
+    if y_work is None:
+        y_work = torch.empty_like(x)
+    if q_out is None:
+        q_out = torch.empty((M, d), dtype=torch.uint8, device=x.device)
+    if scale_out is None:
+        scale_out = torch.empty((M,), dtype=torch.float32, device=x.device)
+    code = lib().sptp_prologue_e4m3(_ptr(x), _ptr(partials), _ptr(gamma), M, d, P, float(eps), _ptr(h_out),
+                                    _ptr(y_work), _ptr(q_out), _ptr(scale_out), _stream(stream))
+    _check("sptp_prologue_e4m3", code)
+    return h_out, q_out, scale_out
 
 
 def sptp_gateup_swiglu_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, P, s_out=None, workspace=None, stream=None):

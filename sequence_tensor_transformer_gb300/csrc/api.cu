@@ -1059,7 +1059,7 @@ int sptp_ffn_forward_fp8(const void* x, const void* partials, const void* gamma,
     const int band = band_for_chunks(M, chunks);
     const int f = F / P;
 
-    // 1-3: partial sum, residual add, RMSNorm -> the bf16 activation y
+    // 1-3: partial sum, residual add, RMSNorm -> the bf16 activation y ...
     PrologueParams pp;
     std::memset(&pp, 0, sizeof(pp));
     pp.G = 1;
@@ -1071,9 +1071,10 @@ int sptp_ffn_forward_fp8(const void* x, const void* partials, const void* gamma,
     for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
     pp.status = st;
     pp.wait_limit_ns = kWaitLimitNs;
+    // ... and the gate/up linear's quantisation of y per token, fused
+    pp.q = qy;
+    pp.qscale = sy;
     if ((rc = cuda_status(launch_prologue(pp, true, di.sms, s))) != SPTP_OK) return rc;
-    // the gate/up linear quantises its input per token
-    if ((rc = cuda_status(launch_quantize_rows_e4m3(y, M, d, qy, sy, di.sms, s))) != SPTP_OK) return rc;
     // 4-6: (identity) gather + column-parallel E4M3 gate/up + SwiGLU
     if ((rc = gateup_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, M, d, F, P, sbuf, st, band, di, s)) != SPTP_OK) return rc;
     // the down linear quantises s per token within each shard
@@ -1084,6 +1085,47 @@ int sptp_ffn_forward_fp8(const void* x, const void* partials, const void* gamma,
     void* outs[kMaxGroups];
     for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * act);
     return down_e4m3(qs, ss, qW2, sW2, M, d, F, P, outs, st, band, di, s);
+}
+
+int sptp_prologue_e4m3(const void* x, const void* partials, const void* gamma, int M, int d, int P, float eps,
+                       void* h_out, void* y_work, void* q_out, float* scale_out, void* cuda_stream) {
+    if (!gamma || (M != 0 && (!x || !partials || !y_work || !q_out || !scale_out))) return SPTP_ERR_NULL;
+    int rc = check_common(M, d, 8 * P, P, SPTP_BF16);
+    if (rc != SPTP_OK) return rc;
+    if (d % 16 != 0 || !(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
+    const void* ptrs[] = {x, partials, gamma, h_out, y_work, q_out, scale_out};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
+    const size_t act = static_cast<size_t>(M) * d * 2;
+    const void* ins[] = {x, partials, gamma, h_out};
+    const size_t insz[] = {act, act * P, static_cast<size_t>(d) * 2, h_out ? act : 0};
+    void* outs[] = {y_work, q_out, scale_out};
+    const size_t osz[] = {act, act / 2, static_cast<size_t>(M) * 4};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(outs[o], osz[o], ins[i], insz[i])) return SPTP_ERR_ALIAS;
+        for (int j = o + 1; j < 3; ++j)
+            if (overlaps(outs[o], osz[o], outs[j], osz[j])) return SPTP_ERR_ALIAS;
+    }
+    if (h_out && h_out != x && (overlaps(h_out, act, partials, act * P) || overlaps(h_out, act, x, act)))
+        return SPTP_ERR_ALIAS;
+    if (M == 0) return SPTP_OK;
+    DevInfo di;
+    if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    PrologueParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.G = 1;
+    pp.M = M;
+    pp.d = d;
+    pp.eps = eps;
+    pp.gamma = gamma;
+    pp.grp[0] = PrologueGroup{x, h_out, y_work, 0, P};
+    for (int p = 0; p < P; ++p) pp.src[p] = cptr(partials, static_cast<size_t>(p) * act);
+    pp.status = nullptr;
+    pp.wait_limit_ns = kWaitLimitNs;
+    pp.q = q_out;
+    pp.qscale = scale_out;
+    return cuda_status(launch_prologue(pp, true, di.sms, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 int sptp_gateup_swiglu_e4m3(const void* qy, const float* sy, const void* qW1g, const float* sW1g, const void* qW1u,

@@ -12,6 +12,15 @@
 //               convert, 16-byte global stores; overlaps the next tile's MMAs
 // Tiles are walked in raster bands of `band` m-tiles (a sequence chunk) so
 // that concurrently running CTAs share A and B tiles in L2.
+//
+// The CTA-pair kernel (namespace pair, cta_group::2) is the default: tiles of
+// 256 rows x 256 B rows, each CTA of a cluster pair staging its own 128 rows
+// of A and of B, one MMA thread on the even CTA, six 32 KiB stages.  It runs
+// on bf16 operands (kind::f16, 64 elements per 128-byte row) or on E4M3
+// operands (kind::f8f6f4, 128 per row) for the fp8 linear layers ("[Feature]
+// Async Tensor Parallelism for Archon Engine", "Additional Information"),
+// whose epilogue multiplies the fp32 accumulator by the token row's and the
+// output column's power-of-two scales.
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
@@ -277,11 +286,13 @@ namespace pair {
 
 constexpr int PBM = 256;                     // tile rows (128 per CTA)
 constexpr int PBN = 256;                     // UMMA N
-constexpr int PSTAGES = 6;
+constexpr int kMaxPStages = 7;              // 7 x 32 KiB + barriers still fits in 227 KiB
 constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
 constexpr int B_BYTES = 128 * BK * 2;        // 16 KiB (half of the B tile)
 constexpr int PSTAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int PSMEM_BYTES = 1024 + PSTAGES * PSTAGE_BYTES + BAR_BYTES;
+template <int ST>
+constexpr int psmem_bytes() { return 1024 + ST * PSTAGE_BYTES + BAR_BYTES; }
+static_assert(psmem_bytes<kMaxPStages>() <= 227 * 1024, "pipeline does not fit in shared memory");
 // A stage holds 128-byte K slices of each operand row: 64 bf16 or 128 E4M3
 // elements.  Either way 4 UMMAs of 32 bytes per row consume it.
 template <bool E4M3>
@@ -321,8 +332,8 @@ __device__ __forceinline__ void load_col_scales_strided(const float* sc, int str
 }
 
 struct Bars {
-    uint64_t full[PSTAGES];
-    uint64_t empty[PSTAGES];
+    uint64_t full[kMaxPStages];
+    uint64_t empty[kMaxPStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -331,7 +342,7 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= BAR_BYTES, "barrier block too large");
 
-template <Epi EPI, int EW, bool E4M3>
+template <Epi EPI, int EW, bool E4M3, int PSTAGES>
 __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
     constexpr int KE = k_elems<E4M3>();
     extern __shared__ uint8_t smem_raw[];
@@ -656,10 +667,11 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStre
 
 namespace {
 
-template <Epi EPI, int EW, bool E4M3 = false>
+template <Epi EPI, int EW, bool E4M3 = false, int ST = 6>
 cudaError_t launch_pair_typed(const TcGemmParams& p, int num_sms, cudaStream_t s) {
-    auto* kfn = pair::tc_gemm_pair_kernel<EPI, EW, E4M3>;
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, pair::PSMEM_BYTES);
+    auto* kfn = pair::tc_gemm_pair_kernel<EPI, EW, E4M3, ST>;
+    constexpr int PSMEM_BYTES = pair::psmem_bytes<ST>();
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -668,7 +680,7 @@ cudaError_t launch_pair_typed(const TcGemmParams& p, int num_sms, cudaStream_t s
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(pair::pair_threads<EW>(), 1, 1);
-    cfg.dynamicSmemBytes = pair::PSMEM_BYTES;
+    cfg.dynamicSmemBytes = PSMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -705,6 +717,8 @@ cudaError_t launch_tc_gemm_pair(const TcGemmParams& p, Epi epi, int num_sms, cud
 
 cudaError_t launch_tc_gemm_pair_e4m3(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s) {
     if (p.G * p.mt * p.nt == 0) return cudaSuccess;
+    // six stages, as for bf16: a seventh measured no faster for either
+    // operand type (8192 x 4096 x 14336: E4M3 step 2824 vs 2824 TFLOP/s)
     return epi == Epi::kSwiGLU ? launch_pair_typed<Epi::kSwiGLU, 4, true>(p, num_sms, s)
                                : launch_pair_typed<Epi::kStore, 4, true>(p, num_sms, s);
 }

@@ -12,6 +12,7 @@
 // h = x + r; the norm uses the unrounded fp32 h.
 #include <cuda_bf16.h>
 
+#include "e4m3.cuh"
 #include "sptp_ptx.cuh"
 
 namespace sptp {
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(1024) prologue_rows(const __grid_constant__ Pr
                     float gm[E];
                     V::load(p.gamma, col, gm);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) gm[e] = h[v][e] * inv * gm[e];
+                    for (int e = 0; e < E; ++e) gm[e] = (h[v][e] * gm[e]) * inv;
                     V::store(grpd.y, off + col, gm);
                 }
             }
@@ -197,14 +198,22 @@ struct TmaLayout {
     uint32_t row_bytes; // d * sizeof(T)
 };
 
-template <typename T, int VPT>
+//
+// y_j = (h_j * gamma_j) * rsqrt(mean h^2 + eps), each product rounded to fp32.
+// QUANT (bf16, one group): instead of y, write y's E4M3 codes and row scale
+// (codes of y * 2^-e, e from the row maximum A of the bf16 y).  Rounding is
+// monotone and sign-symmetric, so A = bf16(m * rsqrt) exactly, with
+// m = max_j |h_j * gamma_j|: m joins the first block reduction and the row
+// needs no second barrier.
+template <typename T, int VPT, bool QUANT>
 __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ PrologueParams p, TmaLayout L) {
     using V = Vec<T>;
     constexpr int E = V::E;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     __shared__ uint64_t full[kTmaMaxStages];
-    __shared__ float red[2][16];
+    __shared__ __align__(16) float red[2][16];
+    __shared__ __align__(16) float red_mg[2][16];
     __shared__ int abort_flag;
     const int nthr = blockDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
@@ -261,8 +270,9 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
         const long long row = gr - static_cast<long long>(g) * p.M;
         const PrologueGroup& grp = p.grp[g];
         const uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
-        float h[VPT][E];
-        float ss = 0.f;
+        const long long off = row * d;
+        float hg[VPT][E];  // h * gamma; h itself is stored at once
+        float ss = 0.f, mg = 0.f;
         if (ok) {
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
@@ -277,18 +287,27 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
 #pragma unroll
                         for (int e = 0; e < E; ++e) r[e] += u[e];
                     }
-                    float xv[E];
-                    V::load_smem(st, col, xv);
+                    float hv[E];
+                    V::load_smem(st, col, hv);
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
-                        h[v][e] = xv[e] + r[e];
-                        ss = fmaf(h[v][e], h[v][e], ss);
+                        hv[e] += r[e];
+                        ss = fmaf(hv[e], hv[e], ss);
+                        hg[v][e] = hv[e] * gm[v][e];
+                        if constexpr (QUANT) mg = fmaxf(mg, fabsf(hg[v][e]));
                     }
+                    // h (the new residual, a final output) needs no norm
+                    if (grp.h != nullptr) V::store_stream(grp.h, off + col, hv);
                 }
             }
         }
         ss = warp_sum(ss);
         if (lane == 0) red[parity][warp] = ss;
+        if constexpr (QUANT) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+            if (lane == 0) red_mg[parity][warp] = mg;
+        }
         __syncthreads();
         if (abort_flag) break;  // uniform: written before the barrier
         if (tid == 0 && i + L.S < my_rows) {
@@ -297,22 +316,60 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
             fence_proxy_async_smem();
             issue(i + L.S);
         }
+        // the per-warp values in ascending warp order (16-byte reads)
         ss = 0.f;
-        for (int w = 0; w < nwarps; ++w) ss += red[parity][w];
+        if ((nwarps & 3) == 0) {
+            for (int w = 0; w < nwarps; w += 4) {
+                const float4 q4 = *reinterpret_cast<const float4*>(&red[parity][w]);
+                ss = (((ss + q4.x) + q4.y) + q4.z) + q4.w;
+                if constexpr (QUANT) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(&red_mg[parity][w]);
+                    mg = fmaxf(mg, fmaxf(fmaxf(m4.x, m4.y), fmaxf(m4.z, m4.w)));
+                }
+            }
+        } else {
+            for (int w = 0; w < nwarps; ++w) {
+                ss += red[parity][w];
+                if constexpr (QUANT) mg = fmaxf(mg, red_mg[parity][w]);
+            }
+        }
         parity ^= 1;
         const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
-        const long long off = row * d;
+        if constexpr (!QUANT) {
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int col = (v * nthr + tid) * E;
-            if (col < d) {
-                if (grp.h != nullptr) V::store_stream(grp.h, off + col, h[v]);
-                if (grp.y != nullptr) {
-                    float yv[E];
+            for (int v = 0; v < VPT; ++v) {
+                const int col = (v * nthr + tid) * E;
+                if (col < d) {
+                    if (grp.y != nullptr) {
+                        float yv[E];
 #pragma unroll
-                    for (int e = 0; e < E; ++e) yv[e] = h[v][e] * inv * gm[v][e];
-                    V::store(grp.y, off + col, yv);
+                        for (int e = 0; e < E; ++e) yv[e] = hg[v][e] * inv;
+                        V::store(grp.y, off + col, yv);
+                    }
                 }
+            }
+        } else {
+            static_assert(E == 8, "bf16 rows only");
+            // the bf16 activation y
+            uint4 yb[VPT];
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int col = (v * nthr + tid) * E;
+                if (col < d) {
+                    __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&yb[v]);
+#pragma unroll
+                    for (int e = 0; e < E / 2; ++e)
+                        b2[e] = __floats2bfloat162_rn(hg[v][2 * e] * inv, hg[v][2 * e + 1] * inv);
+                }
+            }
+            const int ex = e4m3_row_exponent(__bfloat162float(__float2bfloat16_rn(mg * inv)));
+            const float qinv = pow2f(-ex);
+            if (tid == 0) p.qscale[row] = pow2f(ex);
+            uint8_t* qrow = static_cast<uint8_t*>(p.q) + off;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int col = (v * nthr + tid) * E;
+                if (col < d) *reinterpret_cast<uint2*>(qrow + col) = e4m3_quant8(yb[v], qinv);
             }
         }
     }
@@ -325,10 +382,10 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
     }
 }
 
-template <typename T, int VPT>
+template <typename T, int VPT, bool QUANT = false>
 cudaError_t launch_tma(const PrologueParams& p, const TmaLayout& L, int threads, int num_sms, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(L.S) * L.row_bytes * (L.max_src + 1) + 128;
-    cudaError_t e = cudaFuncSetAttribute(prologue_tma<T, VPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prologue_tma<T, VPT, QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const long long rows = static_cast<long long>(p.G) * p.M;
@@ -339,7 +396,7 @@ cudaError_t launch_tma(const PrologueParams& p, const TmaLayout& L, int threads,
     if (per_sm < 1) per_sm = 1;
     long long grid = static_cast<long long>(num_sms) * per_sm;
     if (grid > rows) grid = rows;
-    prologue_tma<T, VPT><<<static_cast<int>(grid), threads, smem, s>>>(p, L);
+    prologue_tma<T, VPT, QUANT><<<static_cast<int>(grid), threads, smem, s>>>(p, L);
     return cudaGetLastError();
 }
 
@@ -362,6 +419,14 @@ cudaError_t launch_typed(const PrologueParams& p, int num_sms, cudaStream_t s) {
     const int vpt = (nvec + threads - 1) / threads;
     if (S >= 2 && vpt <= 8) {
         TmaLayout L{S, max_src, static_cast<uint32_t>(p.d * sizeof(T))};
+        if constexpr (sizeof(T) == 2) {
+            if (p.q != nullptr) {
+                if (vpt <= 1) return launch_tma<T, 1, true>(p, L, threads, num_sms, s);
+                if (vpt <= 2) return launch_tma<T, 2, true>(p, L, threads, num_sms, s);
+                if (vpt <= 4) return launch_tma<T, 4, true>(p, L, threads, num_sms, s);
+                return launch_tma<T, 8, true>(p, L, threads, num_sms, s);
+            }
+        }
         if (vpt <= 1) return launch_tma<T, 1>(p, L, threads, num_sms, s);
         if (vpt <= 2) return launch_tma<T, 2>(p, L, threads, num_sms, s);
         if (vpt <= 4) return launch_tma<T, 4>(p, L, threads, num_sms, s);
@@ -383,12 +448,18 @@ cudaError_t launch_typed(const PrologueParams& p, int num_sms, cudaStream_t s) {
     if (vptr == 1) prologue_rows<T, 1><<<g, block, smem, s>>>(p, tpr, R);
     else if (vptr == 2) prologue_rows<T, 2><<<g, block, smem, s>>>(p, tpr, R);
     else prologue_rows<T, 4><<<g, block, smem, s>>>(p, tpr, R);
-    return cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
+    // rows too wide for the fused quantisation: quantise the stored y
+    if (e == cudaSuccess && p.q != nullptr)
+        e = launch_quantize_rows_e4m3(p.grp[0].y, p.M, p.d, p.q, p.qscale, num_sms, s);
+    return e;
 }
 
 }  // namespace
 
 cudaError_t launch_prologue(const PrologueParams& p, bool bf16, int num_sms, cudaStream_t s) {
+    if (p.q != nullptr && (!bf16 || p.G != 1 || p.grp[0].y == nullptr || p.qscale == nullptr))
+        return cudaErrorInvalidValue;
     return bf16 ? launch_typed<__nv_bfloat16>(p, num_sms, s) : launch_typed<float>(p, num_sms, s);
 }
 

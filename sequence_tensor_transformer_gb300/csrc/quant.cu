@@ -11,9 +11,7 @@
 // up to kCached 16-byte vectors of its row in registers between the
 // row-maximum pass and the quantise pass, so a row of up to 8192 elements is
 // read once.  Longer rows re-read the rest (from L2).
-#include <cuda_bf16.h>
-#include <cuda_fp8.h>
-
+#include "e4m3.cuh"
 #include "sptp_internal.h"
 
 namespace sptp {
@@ -22,41 +20,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCached = 4;
-
-__device__ __forceinline__ float absmax8(const uint4 v) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-    __nv_bfloat162 m = __habs2(h[0]);
-    m = __hmax2(m, __habs2(h[1]));
-    m = __hmax2(m, __habs2(h[2]));
-    m = __hmax2(m, __habs2(h[3]));
-    return fmaxf(__low2float(m), __high2float(m));
-}
-
-// e = least integer >= -126 with amax <= 448 * 2^e.  With amax = 1.m * 2^E
-// (normal), 448 = 1.75 * 2^8: e = E - 8, plus one when 1.m > 1.75.
-__device__ __forceinline__ int row_exponent(float amax) {
-    const uint32_t u = __float_as_uint(amax);
-    const int biased = static_cast<int>(u >> 23);  // amax >= 0
-    const int e = biased - 127 - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-    return biased == 0 ? -126 : max(e, -126);
-}
-
-__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
-
-// 8 bf16 -> 8 E4M3 bytes, each scaled by inv (a power of two)
-__device__ __forceinline__ uint2 quant8(const uint4 v, float inv) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-    uint32_t w[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float2 a = __bfloat1622float2(h[2 * i]);
-        const float2 b = __bfloat1622float2(h[2 * i + 1]);
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a.x * inv, a.y * inv), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(b.x * inv, b.y * inv), __NV_SATFINITE, __NV_E4M3);
-        w[i] = (lo & 0xFFFFu) | (hi << 16);
-    }
-    return make_uint2(w[0], w[1]);
-}
 
 __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint4* __restrict__ a, long long R,
                                                                       int nvec, uint2* __restrict__ q,
@@ -72,11 +35,11 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint
             const int idx = threadIdx.x + i * kThreads;
             if (idx < nvec) {
                 v[i] = __ldcs(src + idx);
-                amax = fmaxf(amax, absmax8(v[i]));
+                amax = fmaxf(amax, absmax_bf16x8(v[i]));
             }
         }
         for (int idx = threadIdx.x + kCached * kThreads; idx < nvec; idx += kThreads)
-            amax = fmaxf(amax, absmax8(__ldg(src + idx)));
+            amax = fmaxf(amax, absmax_bf16x8(__ldg(src + idx)));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
@@ -85,16 +48,16 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint
 #pragma unroll
         for (int w = 1; w < kThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
         __syncthreads();  // warp_max is reused by the next row
-        const int e = row_exponent(amax);
+        const int e = e4m3_row_exponent(amax);
         const float inv = pow2f(-e);
         if (threadIdx.x == 0) scale[r] = pow2f(e);
 #pragma unroll
         for (int i = 0; i < kCached; ++i) {
             const int idx = threadIdx.x + i * kThreads;
-            if (idx < nvec) dst[idx] = quant8(v[i], inv);
+            if (idx < nvec) dst[idx] = e4m3_quant8(v[i], inv);
         }
         for (int idx = threadIdx.x + kCached * kThreads; idx < nvec; idx += kThreads)
-            dst[idx] = quant8(__ldg(src + idx), inv);
+            dst[idx] = e4m3_quant8(__ldg(src + idx), inv);
     }
 }
 

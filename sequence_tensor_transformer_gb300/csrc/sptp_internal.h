@@ -58,6 +58,12 @@ struct PrologueParams {
     float eps;
     DeviceStatus* status;            // may be null (no status words)
     unsigned long long wait_limit_ns;
+    // bf16, G == 1 only: when q != nullptr the bf16 y is also quantised row-wise
+    // to E4M3 codes q [M][d] with power-of-two scales qscale [M] (grp[0].y
+    // must still be given: rows too wide for the fused path are written there
+    // and quantised by a second launch)
+    void* q;
+    float* qscale;
 };
 
 // Launches the partial-sum + residual + RMSNorm kernel over G groups of M rows.

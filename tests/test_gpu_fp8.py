@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import sequence_tensor_transformer_gb300 as st
 from oracle import fp8_oracle as f8
 from sequence_tensor_transformer_gb300 import synth
@@ -97,6 +98,30 @@ def test_weight_quantisation_layout_bit_exact():
     assert got[5].shape == (d, P)
 
 
+@pytest.mark.parametrize("M,d,P", [(1, 16, 1), (37, 144, 2), (300, 1024, 3), (129, 4096, 2), (64, 5120, 4),
+                                   (16, 8192, 8)])
+def test_prologue_e4m3_equals_prologue_then_quantiser(M, d, P):
+    """The fused launch gives the codes of quantising the prologue's own y
+    (bit for bit), and they dequantise to within one E4M3 rounding of the
+    oracle's bf16 y.  d=8192 with 8 sources takes the two-launch fallback."""
+    rng = np.random.default_rng(M * 7 + d)
+    x, parts = bf16_array(rng, (M, d)), bf16_array(rng, (P, M, d))
+    gamma = synth._cast(1 + 0.1 * rng.standard_normal(d), "bf16")
+    X, Pt, G = dev_tensor(x, "bf16"), dev_tensor(parts, "bf16"), dev_tensor(gamma, "bf16")
+    h1, q1, s1 = st.sptp_prologue_e4m3(X, Pt, G, 1e-6)
+    h0, y0 = st.sptp_prologue(X, Pt, G, 1e-6)
+    q0, s0 = st.sptp_quantize_rows_e4m3(y0)
+    torch.cuda.synchronize()
+    assert torch.equal(h1, h0) and torch.equal(q1, q0) and torch.equal(s1, s0)
+    href = synth.to_f64(x, "bf16") + synth.to_f64(parts, "bf16").sum(0)
+    yref = f8.round_bf16(oracle.rms_norm(href, synth.to_f64(gamma, "bf16"), 1e-6))
+    sc = s1.cpu().double().numpy()
+    deq = q1.view(torch.float8_e4m3fn).cpu().double().numpy() * sc[:, None]
+    assert np.all(np.abs(deq - yref) <= 0.07 * np.abs(yref) + 2.0 ** -10 * sc[:, None])
+    _, e = f8.quantize_rows_e4m3(yref)
+    assert np.all(np.abs(np.log2(sc) - e) <= 1)
+
+
 # ---------------------------------------------------------------- GEMMs
 
 @pytest.mark.parametrize("M,d,F,P", [(64, 128, 512, 2), (300, 144, 2 * 400, 2), (257, 1024, 3 * 384, 3),
@@ -153,8 +178,10 @@ def case(M, d, F, P, C, seed=0):
 
 @pytest.mark.parametrize("M,d,F,P,C", [(320, 256, 768, 2, 2), (384, 144, 3 * 208, 3, 3),
                                        (1000, 512, 4 * 400, 4, 8), (2048, 1024, 8 * 256, 8, 8), (130, 64, 64, 1, 1),
-                                       (2, 16, 32, 2, 2)])
+                                       (2, 16, 32, 2, 2), (64, 8192, 8 * 128, 8, 8)])
 def test_boundary_fp8_multi_tile_and_ragged(M, d, F, P, C):
+    # d=8192 with 8 sources: rows too wide for the prologue's shared-memory
+    # ring, so y is stored and quantised by a second launch
     run_fp8(case(M, d, F, P, C))
 
 
