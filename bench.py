@@ -613,7 +613,7 @@ def _fp8_line(args, cfg, to_dev, dev, stream, pk):
     # nominal fp8 / bf16 dense ratio (4.5 / 2.25)
     fp8_peak = 2.0 * pk["bf16_burst"]
     value = 6.0 * M * d * F / (ms * 1e-3) / 1e12
-    kernels = {name: {"ms": t} for name, t in k.items()}
+    kernels = {name: {"ms": t, "traffic": kernel_traffic(name)} for name, t in k.items()}
     kernels["gateup_e4m3"]["achieved_tflops"] = fl_gu / (k["gateup_e4m3"] * 1e-3) / 1e12
     kernels["down_e4m3"]["achieved_tflops"] = fl_dn / (k["down_e4m3"] * 1e-3) / 1e12
     kernels["quantize_s"]["achieved_gbs"] = (3.0 * P * M * f + 4.0 * P * M) / (k["quantize_s"] * 1e-3) / 1e9
@@ -628,7 +628,7 @@ def _fp8_line(args, cfg, to_dev, dev, stream, pk):
                         "weights": "E4M3 + row scales, quantised once outside the timed region"},
                 weight_quantisation_ms=ms_wq, kernels=kernels,
                 roofline={"bound": "tensor", "kernel": "gateup_e4m3", "achieved": gu, "peak": fp8_peak,
-                          "unit": "TFLOP/s", "frac": gu / fp8_peak,
+                          "unit": "TFLOP/s", "frac": gu / fp8_peak, "traffic": kernel_traffic("gateup_e4m3"),
                           "peak_note": "2 x measured burst bf16 (nominal fp8:bf16 dense ratio); the whole step "
                                        "against 2 x sustained bf16: %.3f" % (value / (2.0 * pk["bf16_sustained"]))})
 
