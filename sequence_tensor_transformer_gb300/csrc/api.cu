@@ -287,6 +287,13 @@ bool dtp_fused_selected() {
 // With SPTP_STRICT_VARIANT=1 a selected fused launch that cannot run is an
 // error (SPTP_ERR_CUDA) instead of a fall-back to the multi-launch path; the
 // tests use it to make sure the variant they name is the one that ran.
+// The attention-side boundary as one fused launch: SPTP_ATTN_VARIANT=fused
+// (else prologue + column-parallel GEMM).
+bool attn_fused_selected() {
+    const char* v = std::getenv("SPTP_ATTN_VARIANT");
+    return v != nullptr && std::strcmp(v, "fused") == 0;
+}
+
 bool strict_variant() {
     const char* v = std::getenv("SPTP_STRICT_VARIANT");
     return v != nullptr && std::strcmp(v, "1") == 0;
@@ -482,6 +489,73 @@ int fused_forward(const void* x, const void* partials, const void* gamma, const 
     if (e == cudaSuccess) return SPTP_OK;
     // A launch that the runtime rejects (for example a cooperative cluster
     // launch it does not support) enqueues nothing; use the three-launch path.
+    cudaGetLastError();
+    if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidValue || e == cudaErrorNotSupported ||
+        e == cudaErrorInvalidConfiguration) {
+        unavailable[dev & 63] = true;
+        return SPTP_ERR_UNSUPPORTED;
+    }
+    return SPTP_ERR_CUDA;
+}
+
+// The bf16 boundary in front of attention as one persistent launch
+// (fused.cu with qkv set: prologue rows feed each shard's column-parallel QKV
+// GEMM).  Returns SPTP_ERR_UNSUPPORTED, having enqueued nothing, where it
+// cannot launch.
+int fused_attn_forward(const void* x, const void* partials, const void* gamma, const void* Wqkv, int M, int d,
+                       int N, int P, int chunks, float eps, void* qkv_out, void* resid_out, void* y, int* counters,
+                       DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
+    static bool unavailable[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (unavailable[dev & 63]) return SPTP_ERR_UNSUPPORTED;
+    const int max_pairs = fused_max_pairs(di.sms);
+    if (max_pairs <= 0) {
+        unavailable[dev & 63] = true;
+        return SPTP_ERR_UNSUPPORTED;
+    }
+    const size_t es = 2;
+    const int n = N / P;
+    const size_t act = static_cast<size_t>(M) * d * es;
+    FusedParams p;
+    std::memset(&p, 0, sizeof(p));
+    bool ok = encode_map_bf16(&p.mapY, y, d, M, static_cast<uint64_t>(d) * es, kBK, kBM);
+    for (int g = 0; g < P && ok; ++g) {
+        ok = encode_map_bf16(&p.mapW1g[g], cptr(Wqkv, static_cast<size_t>(g) * n * d * es), d, n,
+                             static_cast<uint64_t>(d) * es, kBK, kBM);
+        p.s_out[g] = mptr(qkv_out, static_cast<size_t>(g) * M * n * es);
+        p.partials[g] = cptr(partials, static_cast<size_t>(g) * act);
+    }
+    if (!ok) return SPTP_ERR_CUDA;
+    p.x = x;
+    p.gamma = gamma;
+    p.h_out = resid_out;
+    p.y = y;
+    p.eps = eps;
+    p.M = M;
+    p.d = d;
+    p.P = P;
+    p.f = n;
+    p.qkv = 1;
+    p.mt = (M + 255) / 256;
+    p.nt_gu = (n + kBNStore - 1) / kBNStore;
+    p.nk_gu = (d + kBK - 1) / kBK;
+    const int pband = (band + 1) / 2;
+    p.band = pband < 1 ? 1 : (pband > p.mt ? p.mt : pband);
+    const int chunk_rows = M / chunks;
+    const int first_rows = chunk_rows > kFirstBandRows ? chunk_rows : kFirstBandRows;
+    const int first_tiles = first_rows / 256;
+    p.band0 = first_tiles < 1 ? 1 : (first_tiles > p.band ? p.band : first_tiles);
+    p.tiles_gu = P * p.mt * p.nt_gu;
+    p.tiles_dn = 0;
+    p.rb_ready = counters;
+    p.gu_done = counters;  // unused without down tiles
+    p.status = st;
+    p.wait_limit_ns = kWaitLimitNs;
+    const int pairs = p.tiles_gu < max_pairs ? p.tiles_gu : max_pairs;
+    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(p.mt) * sizeof(int), s) != cudaSuccess) return SPTP_ERR_CUDA;
+    const cudaError_t e = launch_boundary_fused(p, pairs, s);
+    if (e == cudaSuccess) return SPTP_OK;
     cudaGetLastError();
     if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidValue || e == cudaErrorNotSupported ||
         e == cudaErrorInvalidConfiguration) {
@@ -874,7 +948,8 @@ int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P,
 
 size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, int dtype) {
     if (check_common(M, d, N, P, dtype) != SPTP_OK || chunks < 1) return 0;
-    return SPTP_WS_HEADER_BYTES + align_up(static_cast<size_t>(M) * d * esize(dtype));
+    return SPTP_WS_HEADER_BYTES + align_up(static_cast<size_t>(M) * d * esize(dtype)) +
+           align_up(static_cast<size_t>((M + 255) / 256) * sizeof(int));
 }
 
 int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma, const void* Wqkv, int M, int d,
@@ -914,6 +989,13 @@ int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     void* y = mptr(workspace, SPTP_WS_HEADER_BYTES);
+    int* counters = reinterpret_cast<int*>(mptr(workspace, SPTP_WS_HEADER_BYTES + align_up(act)));
+    if (dtype == SPTP_BF16 && attn_fused_selected()) {
+        rc = fused_attn_forward(x, partials, gamma, Wqkv, M, d, N, P, chunks, eps, qkv_out, resid_out, y, counters,
+                                ws_status(workspace), band_for_chunks(M, chunks), di, s);
+        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
+        if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: prologue + GEMM below
+    }
     PrologueParams pp;
     std::memset(&pp, 0, sizeof(pp));
     pp.G = 1;

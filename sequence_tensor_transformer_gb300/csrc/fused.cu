@@ -21,6 +21,11 @@
 // tiles), then all down tiles; pair q takes tiles q, q + npairs, ...  Every
 // dependency points to work earlier in that order or to prologue rows, which
 // never wait, so with all CTAs resident every wait ends.
+//
+// With p.qkv set the same launch is the boundary in front of an attention
+// sub-layer (the pages' 4 boundaries per block): the prologue rows feed a
+// column-parallel store GEMM of each shard's Wqkv rows instead of gate/up,
+// and there are no down tiles.
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
@@ -131,32 +136,47 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // h = x + (0 + partial_0 + partial_1 + ...) for NV 8-column vectors of one
-// row, 256 columns apart (vectors past d are left untouched); the loads of
-// one source for all NV vectors are issued together.  h accumulates the
-// partials first and x last (one IEEE addition per element, so h + x equals
-// x + h bit for bit).
+// row, 256 columns apart (vectors past d are left untouched).  The loads of
+// kSrcBatch sources x NV vectors are issued together before any is used
+// (8 16-byte loads in flight per lane), then added in source order.  (One
+// source at a time, 2 x 4 and 5 x 2 measured: the attention-side boundary's
+// rows 573 / 517 / 495 us, the FFN boundary 1646 / 1653 / 1623 TFLOP/s.)  h
+// accumulates the partials first and x last (one IEEE addition per element,
+// so h + x equals x + h bit for bit).
+constexpr int kSrcBatch = 2;
+
 template <int NV>
 __device__ __forceinline__ void row_h(const FusedParams& p, long long row_off, int col0, float (&h)[NV][8]) {
 #pragma unroll
     for (int v = 0; v < NV; ++v)
 #pragma unroll
         for (int e = 0; e < 8; ++e) h[v][e] = 0.f;
-    for (int q = 0; q <= p.P; ++q) {
-        const __nv_bfloat16* src = q < p.P ? static_cast<const __nv_bfloat16*>(p.partials[q])
-                                           : static_cast<const __nv_bfloat16*>(p.x);
-        uint4 u[NV];
+    for (int q0 = 0; q0 <= p.P; q0 += kSrcBatch) {
+        uint4 u[kSrcBatch][NV];
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
-            if (col0 + 256 * v < p.d) u[v] = __ldg(reinterpret_cast<const uint4*>(src + row_off + col0 + 256 * v));
+        for (int b = 0; b < kSrcBatch; ++b) {
+            const int q = q0 + b;
+            if (q > p.P) break;
+            const __nv_bfloat16* src = q < p.P ? static_cast<const __nv_bfloat16*>(p.partials[q])
+                                               : static_cast<const __nv_bfloat16*>(p.x);
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            if (col0 + 256 * v < p.d) {
-                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[v]);
+            for (int v = 0; v < NV; ++v)
+                if (col0 + 256 * v < p.d)
+                    u[b][v] = __ldg(reinterpret_cast<const uint4*>(src + row_off + col0 + 256 * v));
+        }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float2 f2 = __bfloat1622float2(h2[i]);
-                    h[v][2 * i] += f2.x;
-                    h[v][2 * i + 1] += f2.y;
+        for (int b = 0; b < kSrcBatch; ++b) {
+            if (q0 + b > p.P) break;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                if (col0 + 256 * v < p.d) {
+                    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[b][v]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f2 = __bfloat1622float2(h2[i]);
+                        h[v][2 * i] += f2.x;
+                        h[v][2 * i + 1] += f2.y;
+                    }
                 }
             }
         }
@@ -193,6 +213,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
         tma_prefetch_map(&p.mapY);
         for (int g = 0; g < p.P; ++g) {
             tma_prefetch_map(&p.mapW1g[g]);
+            if (p.qkv) continue;  // the other maps are unset
             tma_prefetch_map(&p.mapW1u[g]);
             tma_prefetch_map(&p.mapS[g]);
             tma_prefetch_map(&p.mapW2[g]);
@@ -277,8 +298,12 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             fence_proxy_async_global();
             const int nk = tl.down ? p.nk_dn : p.nk_gu;
             const CUtensorMap* mA = tl.down ? &p.mapS[tl.g] : &p.mapY;
-            const CUtensorMap* mB = tl.down ? &p.mapW2[tl.g] : (rank == 0 ? &p.mapW1g[tl.g] : &p.mapW1u[tl.g]);
-            const int brow = tl.down ? tl.n * PBN + static_cast<int>(rank) * 128 : tl.n * 128;
+            // B: a gate/up tile's halves are gate and up rows; a down or QKV
+            // tile's are rows n*256 + rank*128 of one matrix
+            const bool split_b = tl.down || p.qkv;
+            const CUtensorMap* mB =
+                tl.down ? &p.mapW2[tl.g] : (p.qkv || rank == 0 ? &p.mapW1g[tl.g] : &p.mapW1u[tl.g]);
+            const int brow = split_b ? tl.n * PBN + static_cast<int>(rank) * 128 : tl.n * 128;
             for (int kb = 0; kb < nk; ++kb) {
                 if (!mbar_wait(&bars->empty[stage], phase ^ 1u, wc, kWhereProducerEmpty, t)) {
                     ok = false;
@@ -365,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             const bool row_ok = row < p.M;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
-            if (!tl.down) {
+            if (!tl.down && !p.qkv) {
                 __nv_bfloat16* out =
                     reinterpret_cast<__nv_bfloat16*>(p.s_out[tl.g]) + static_cast<long long>(row) * p.f;
 #pragma unroll 1
@@ -391,8 +416,10 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     }
                 }
             } else {
-                __nv_bfloat16* out =
-                    reinterpret_cast<__nv_bfloat16*>(p.out[tl.g]) + static_cast<long long>(row) * p.d;
+                // down partials [M][d], or the shard's q, k, v columns [M][f]
+                const int ncols = tl.down ? p.d : p.f;
+                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(tl.down ? p.out[tl.g] : p.s_out[tl.g]) +
+                                     static_cast<long long>(row) * ncols;
 #pragma unroll 1
                 for (int c = 0; c < PBN; c += 16) {
                     uint32_t v16[16];
@@ -406,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     if (row_ok) {
 #pragma unroll
                         for (int v = 0; v < 2; ++v)
-                            if (col + 8 * v < p.d)
+                            if (col + 8 * v < ncols)
                                 __stcs(reinterpret_cast<uint4*>(out + col + 8 * v),
                                        make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
                     }
@@ -414,7 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             }
             tc_fence_before();
             mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
-            if (!tl.down) {
+            if (!tl.down && !p.qkv) {
                 // this CTA's 128 rows of the s tile are stored: publish them
                 // to the down tiles' TMA loads
                 fence_proxy_async_global();

@@ -125,7 +125,8 @@ __global__ void __launch_bounds__(1024) prologue_rows(const __grid_constant__ Pr
          base += static_cast<long long>(gridDim.x) * R) {
         const long long gr = base + grp;
         const bool active = gr < total;
-        const int g = active ? static_cast<int>(gr / p.M) : 0;
+        // no division for one group; a 32-bit one otherwise (G * M < 2^31)
+        const int g = active && p.G > 1 ? static_cast<int>(static_cast<uint32_t>(gr) / static_cast<uint32_t>(p.M)) : 0;
         const long long row = active ? gr - static_cast<long long>(g) * p.M : 0;
         const PrologueGroup& grpd = p.grp[g];
         const long long off = row * d;
@@ -231,13 +232,24 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
     }
     __syncthreads();
 
-    // thread 0: start the copies of this CTA's i-th row into stage i % S
-    auto issue = [&](long long i) {
-        const long long gr = first + i * stride;
-        const int g = static_cast<int>(gr / p.M);
-        const long long row = gr - static_cast<long long>(g) * p.M;
+    // (group, row) of global row gr: no division when there is one group;
+    // otherwise a 32-bit one (G * M < 2^31 is checked at launch)
+    auto locate = [&](long long gr, int& g, long long& row) {
+        if (p.G == 1) {
+            g = 0;
+            row = gr;
+        } else {
+            const uint32_t q = static_cast<uint32_t>(gr) / static_cast<uint32_t>(p.M);
+            g = static_cast<int>(q);
+            row = gr - static_cast<long long>(q) * p.M;
+        }
+    };
+    // thread 0: start the copies of this CTA's i-th row into stage s (= i % S)
+    auto issue = [&](long long i, int s) {
+        int g;
+        long long row;
+        locate(first + i * stride, g, row);
         const PrologueGroup& grp = p.grp[g];
-        const int s = static_cast<int>(i % L.S);
         uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
         mbar_arrive_expect_tx(&full[s], slot_bytes * static_cast<uint32_t>(grp.n_src + 1));
         const long long off = row * static_cast<long long>(slot_bytes);
@@ -247,7 +259,7 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
                       static_cast<const uint8_t*>(p.src[grp.src_begin + j]) + off, slot_bytes, &full[s]);
     };
     if (tid == 0)
-        for (long long i = 0; i < L.S && i < my_rows; ++i) issue(i);
+        for (long long i = 0; i < L.S && i < my_rows; ++i) issue(i, static_cast<int>(i));
 
     float gm[VPT][E];
     if (p.gamma != nullptr) {
@@ -260,14 +272,14 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
 
     WaitCtx wc{p.status, &abort_flag, p.wait_limit_ns};
     int parity = 0;
+    int s = 0;           // stage of row i: i % S, kept by counting
+    uint32_t phase = 0;  // (i / S) & 1
     long long i = 0;
     for (; i < my_rows; ++i) {
-        const int s = static_cast<int>(i % L.S);
-        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((i / L.S) & 1), wc, kWherePrologueFull,
-                                  static_cast<int>(i));
-        const long long gr = first + i * stride;
-        const int g = static_cast<int>(gr / p.M);
-        const long long row = gr - static_cast<long long>(g) * p.M;
+        const bool ok = mbar_wait(&full[s], phase, wc, kWherePrologueFull, static_cast<int>(i));
+        int g;
+        long long row;
+        locate(first + i * stride, g, row);
         const PrologueGroup& grp = p.grp[g];
         const uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
         const long long off = row * d;
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
             // every thread has read stage s; order those reads before the
             // copies that overwrite it
             fence_proxy_async_smem();
-            issue(i + L.S);
+            issue(i + L.S, s);
         }
         // the per-warp values in ascending warp order (16-byte reads)
         ss = 0.f;
@@ -372,6 +384,10 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
                 if (col < d) *reinterpret_cast<uint2*>(qrow + col) = e4m3_quant8(yb[v], qinv);
             }
         }
+        if (++s == L.S) {
+            s = 0;
+            phase ^= 1u;
+        }
     }
     if (i < my_rows && tid == 0) {
         // left early: wait (bounded) for copies still in flight into the ring
@@ -405,6 +421,7 @@ cudaError_t launch_typed(const PrologueParams& p, int num_sms, cudaStream_t s) {
     constexpr int E = Vec<T>::E;
     const long long rows = static_cast<long long>(p.G) * p.M;
     if (rows == 0) return cudaSuccess;
+    if (p.G > 1 && rows >= (1ll << 31)) return cudaErrorInvalidValue;  // the kernels' 32-bit row split
     const int nvec = (p.d + E - 1) / E;
 
     // Shared-memory streaming path: rows of all sources staged by bulk copies.

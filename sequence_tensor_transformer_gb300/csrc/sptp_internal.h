@@ -139,6 +139,10 @@ struct FusedParams {
     int mt, nt_gu, nt_dn, nk_gu, nk_dn;   // 256-row tiles
     int band0, band;                      // m-tiles of the first gate/up band, of the others
     int tiles_gu, tiles_dn;
+    // qkv != 0: the boundary in front of attention.  The first tile phase is
+    // a column-parallel store GEMM (B = mapW1g[g], shard g's Wqkv rows [f][d];
+    // output s_out[g] [M][f]) and there is no down phase (tiles_dn == 0).
+    int qkv;
     int* rb_ready;                     // [mt] prologue rows done per 256-row block
     int* gu_done;                      // [P][mt] gate/up tile halves stored
     DeviceStatus* status;

@@ -22,9 +22,15 @@ def _lib():
     torch.cuda.set_device(0)
 
 
-@pytest.fixture(params=["pair", "single"])
+@pytest.fixture(params=["pair", "single", "fused"])
 def gemm_variant(request, monkeypatch):
-    monkeypatch.setenv("SPTP_GEMM_VARIANT", request.param)
+    """Prologue + CTA-pair or single-CTA QKV GEMM, or the whole boundary as one
+    fused persistent launch (SPTP_ATTN_VARIANT=fused; strict mode makes a
+    fall-back an error)."""
+    if request.param == "fused":
+        monkeypatch.setenv("SPTP_ATTN_VARIANT", "fused")
+    else:
+        monkeypatch.setenv("SPTP_GEMM_VARIANT", request.param)
     return request.param
 
 
@@ -50,7 +56,8 @@ def run_qkv(cfg, rows=None):
     assert rel_err(goth, href) <= TOL[cfg.dtype]
 
 
-@pytest.mark.parametrize("M,d,N,P,C", [(300, 136, 3 * 200, 3, 3), (512, 512, 2 * 640, 2, 4), (64, 128, 512, 2, 2)])
+@pytest.mark.parametrize("M,d,N,P,C", [(300, 136, 3 * 200, 3, 3), (512, 512, 2 * 640, 2, 4), (64, 128, 512, 2, 2),
+                                       (2048, 1024, 4 * 1152, 4, 8), (264, 64, 8 * 40, 8, 8)])
 def test_attn_qkv_boundary_bf16(M, d, N, P, C, gemm_variant):
     run_qkv(synth.AttnConfig("t", M, d, N, N // 2, P, C, "bf16"))
 
@@ -59,7 +66,10 @@ def test_attn_qkv_boundary_fp32():
     run_qkv(synth.AttnConfig("t32", 96, 128, 2 * 96, 96, 2, 2, "fp32"))
 
 
-def test_attn_qkv_boundary_qwen2_7b_shape_sampled_rows():
+@pytest.mark.parametrize("variant", ["two_launch", "fused"])
+def test_attn_qkv_boundary_qwen2_7b_shape_sampled_rows(variant, monkeypatch):
+    if variant == "fused":
+        monkeypatch.setenv("SPTP_ATTN_VARIANT", "fused")
     cfg = synth.ATTN_QWEN2_7B_SHAPE
     rng = np.random.default_rng(3)
     rows = sorted(set([0, 1, 255, 256, 8191, cfg.M - 1] + list(rng.choice(cfg.M, 12, replace=False))))
