@@ -574,6 +574,8 @@ int dtp_fused_forward(void* x_shards, const void* gamma, const void* W1g, const 
     int dev = 0;
     cudaGetDevice(&dev);
     if (unavailable[dev & 63]) return SPTP_ERR_UNSUPPORTED;
+    // the kernel numbers prologue rows with 32 bits
+    if (static_cast<long long>(P) * M * (L + 1) >= (1ll << 31)) return SPTP_ERR_UNSUPPORTED;
     const int max_pairs = dtp_fused_max_pairs(di.sms);
     if (max_pairs <= 0) {
         unavailable[dev & 63] = true;
@@ -1022,7 +1024,7 @@ int sptp_permute_ffn_neurons(const void* W1g, const void* W1u, const void* W2, c
     const size_t es = esize(dtype);
     if (static_cast<size_t>(F) * es > 200u * 1024u) return SPTP_ERR_SHAPE;  // one W2 row in shared memory
     if (ws_bytes < SPTP_WS_HEADER_BYTES) return SPTP_ERR_WORKSPACE;
-    const void* ptrs[] = {W1g, W1u, W2, W1g_out, W1u_out, W2_out, workspace};
+    const void* ptrs[] = {W1g, W1u, W2, perm, W1g_out, W1u_out, W2_out, workspace};
     for (const void* q : ptrs)
         if (!aligned16(q)) return SPTP_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(perm) & 3u) != 0) return SPTP_ERR_SHAPE;

@@ -306,20 +306,23 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
 
     if (warp >= PRO_WARP0) {
         // ------------------------------------------------ prologue rows, all steps
-        const long long W = static_cast<long long>(gridDim.x) * PRO_WARPS;
-        const long long per_step = static_cast<long long>(p.P) * p.M;
-        const long long all = per_step * (p.L + 1);
+        // 32-bit row numbering (P * M * (L + 1) < 2^31, checked at launch):
+        // 64-bit divisions per row would cost the warps more than the row
+        const uint32_t W = gridDim.x * PRO_WARPS;
+        const uint32_t per_step = static_cast<uint32_t>(p.P) * static_cast<uint32_t>(p.M);
+        const uint32_t all = per_step * static_cast<uint32_t>(p.L + 1);
+        const uint32_t per_block = static_cast<uint32_t>(p.P) * PBM;
         const int d = p.d;
-        for (long long i = static_cast<long long>(blockIdx.x) * PRO_WARPS + (warp - PRO_WARP0); i < all; i += W) {
+        for (uint32_t i = blockIdx.x * PRO_WARPS + (warp - PRO_WARP0); i < all; i += W) {
             if (*wc.abort_flag) break;
             const int l = static_cast<int>(i / per_step);
-            const long long rem = i - static_cast<long long>(l) * per_step;
+            const uint32_t rem = i - static_cast<uint32_t>(l) * per_step;
             // order inside a step: block m, then shard, then the block's rows
-            const int m = static_cast<int>(rem / (static_cast<long long>(p.P) * PBM));
+            const int m = static_cast<int>(rem / per_block);
             const int rows_m = min(PBM, p.M - m * PBM);
-            const long long idx = rem - static_cast<long long>(m) * p.P * PBM;
-            const int sh = static_cast<int>(idx / rows_m);
-            const long long row = static_cast<long long>(m) * PBM + (idx - static_cast<long long>(sh) * rows_m);
+            const uint32_t idx = rem - static_cast<uint32_t>(m) * per_block;
+            const int sh = static_cast<int>(rows_m == PBM ? idx / PBM : idx / static_cast<uint32_t>(rows_m));
+            const long long row = static_cast<long long>(m) * PBM + (idx - static_cast<uint32_t>(sh) * rows_m);
             if (l >= 1 &&
                 !warp_flag_wait_geq(&p.dn_done[(l - 1) * p.mt + m], 2 * p.P * p.nt_dn, wc, kWhereFusedRows,
                                     static_cast<int>(i)))

@@ -8,7 +8,8 @@
 // HBM-bound gathers, every byte read and written once:
 //   rows    W1g/W1u: one warp per output row, 16-byte coalesced copies
 //   columns W2: a CTA stages up to 8 whole rows in shared memory with
-//           16-byte loads and writes the gathered rows with 16-byte stores
+//           16-byte loads; each output column vector's indices are loaded
+//           once and serve every staged row; 16-byte stores
 // An index outside [0, F) is recorded in the status words and its output is
 // written as zeros; no out-of-range address is formed.
 #include <cuda_bf16.h>
@@ -32,12 +33,11 @@ __device__ void report_bad_index(DeviceStatus* st, int info) {
 __global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t* in0, const uint8_t* in1, uint8_t* out0,
                                                            uint8_t* out1, const int* perm, int L, int F,
                                                            int row_bytes, DeviceStatus* st) {
-    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const uint32_t warps = gridDim.x * (blockDim.x >> 5);
     const int lane = threadIdx.x & 31;
-    const long long total = static_cast<long long>(L) * F;
-    for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
-         w += warps) {
-        const int l = static_cast<int>(w / F);
+    const uint32_t total = static_cast<uint32_t>(L) * static_cast<uint32_t>(F);  // < 2^31, checked at launch
+    for (uint32_t w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += warps) {
+        const int l = static_cast<int>(w / static_cast<uint32_t>(F));
         const int src = perm[w];
         const bool ok = src >= 0 && src < F;
         if (!ok && lane == 0) report_bad_index(st, static_cast<int>(w));
@@ -57,9 +57,11 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t* in0, c
 }
 
 // out[l][r][i] = in[l][r][perm[l][i]]: a CTA stages ROWS consecutive rows of
-// one module in shared memory with 16-byte loads, then each thread gathers 16
-// bytes' worth of consecutive output elements and writes them with one
-// 16-byte store (F * sizeof(T) is a multiple of 16).
+// one module in shared memory with 16-byte loads; then each thread takes
+// output column vectors (16 bytes' worth of consecutive output elements),
+// loads their indices once with 16-byte loads, and gathers and stores that
+// vector for every staged row (F * sizeof(T) is a multiple of 16, and of 32
+// for the index loads).
 template <typename T, int ROWS>
 __global__ void __launch_bounds__(512) permute_cols_kernel(const T* in, T* out, const int* perm, int L, int R, int F,
                                                            DeviceStatus* st) {
@@ -67,36 +69,48 @@ __global__ void __launch_bounds__(512) permute_cols_kernel(const T* in, T* out, 
     T* rows_s = reinterpret_cast<T*>(smem_raw);
     constexpr int E = 16 / sizeof(T);  // elements per 16-byte vector
     const int vec_per_row = F / E;
-    const long long groups = static_cast<long long>(L) * ((R + ROWS - 1) / ROWS);
     const int gpl = (R + ROWS - 1) / ROWS;  // row groups per module
-    for (long long gi = blockIdx.x; gi < groups; gi += gridDim.x) {
-        const int l = static_cast<int>(gi / gpl);
-        const int r0 = static_cast<int>(gi - static_cast<long long>(l) * gpl) * ROWS;
+    const uint32_t groups = static_cast<uint32_t>(L) * static_cast<uint32_t>(gpl);
+    for (uint32_t gi = blockIdx.x; gi < groups; gi += gridDim.x) {
+        const int l = static_cast<int>(gi / static_cast<uint32_t>(gpl));
+        const int r0 = static_cast<int>(gi - static_cast<uint32_t>(l) * gpl) * ROWS;
         const int nr = min(ROWS, R - r0);
         const T* src = in + (static_cast<long long>(l) * R + r0) * F;
         T* dst = out + (static_cast<long long>(l) * R + r0) * F;
         const int* pl = perm + static_cast<long long>(l) * F;
         __syncthreads();  // the previous group is fully gathered
+        const int nvec = nr * vec_per_row;
 #pragma unroll 4
-        for (int v = threadIdx.x; v < nr * vec_per_row; v += blockDim.x)
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x)
             reinterpret_cast<uint4*>(rows_s)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
         __syncthreads();
-#pragma unroll 2
-        for (int v = threadIdx.x; v < nr * vec_per_row; v += blockDim.x) {
-            const int r = v / vec_per_row;
-            const int i0 = (v - r * vec_per_row) * E;
-            union {
-                uint4 u;
-                T e[E];
-            } pack;
+        for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) {
+            int idx[E];
+#pragma unroll
+            for (int k = 0; k < E; k += 4) {
+                const int4 q = __ldg(reinterpret_cast<const int4*>(pl + c * E + k));
+                idx[k] = q.x, idx[k + 1] = q.y, idx[k + 2] = q.z, idx[k + 3] = q.w;
+            }
 #pragma unroll
             for (int k = 0; k < E; ++k) {
-                const int sidx = pl[i0 + k];
-                const bool ok = sidx >= 0 && sidx < F;
-                if (!ok && r0 + r == 0) report_bad_index(st, i0 + k);
-                pack.e[k] = ok ? rows_s[static_cast<long long>(r) * F + sidx] : T(0);
+                const bool ok = idx[k] >= 0 && idx[k] < F;
+                if (!ok) {
+                    if (r0 == 0) report_bad_index(st, c * E + k);
+                    idx[k] = -1;
+                }
             }
-            reinterpret_cast<uint4*>(dst)[v] = pack.u;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) {
+                if (r >= nr) break;
+                const T* row_s = rows_s + static_cast<long long>(r) * F;
+                union {
+                    uint4 u;
+                    T e[E];
+                } pack;
+#pragma unroll
+                for (int k = 0; k < E; ++k) pack.e[k] = idx[k] >= 0 ? row_s[idx[k]] : T(0);
+                reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * F)[c] = pack.u;
+            }
         }
     }
 }
@@ -109,6 +123,7 @@ cudaError_t launch_permute_ffn(const void* W1g, const void* W1u, const void* W2,
     const int es = bf16 ? 2 : 4;
     const long long rows = static_cast<long long>(L) * F;
     if (rows == 0) return cudaSuccess;
+    if (rows >= (1ll << 31)) return cudaErrorInvalidValue;  // the kernels number rows with 32 bits
     long long grid = (rows + 7) / 8;
     if (grid > static_cast<long long>(num_sms) * 8) grid = static_cast<long long>(num_sms) * 8;
     permute_rows_kernel<<<static_cast<int>(grid), 256, 0, s>>>(
