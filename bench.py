@@ -39,10 +39,12 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["boundary", "dtp", "attn", "permute", "fp8"], default="boundary",
+    ap.add_argument("--workload", choices=["boundary", "dtp", "attn", "permute", "fp8", "msweep", "qwen2"],
+                    default="boundary",
                     help="boundary: the SP-TP FFN boundary (the default, headline line); the others measure "
-                         "the Delayed-TP stack, the attention-side boundary, the neuron permutation and the "
-                         "boundary with E4M3 linear layers")
+                         "the Delayed-TP stack, the attention-side boundary, the neuron permutation, the "
+                         "boundary with E4M3 linear layers, the M sweep (d=4096, F=16384, P=8) and the "
+                         "Qwen2-7B-shaped boundary")
     return ap.parse_args()
 
 
@@ -544,6 +546,19 @@ def run_other(args):
                               "frac": value / pk["bf16_sustained"]})
     elif args.workload == "fp8":
         line.update(_fp8_line(args, synth.BOUNDARY_D4096, to_dev, dev, stream, pk))
+    elif args.workload in ("msweep", "qwen2"):
+        cfgs = synth.M_SWEEP if args.workload == "msweep" else (synth.QWEN2_7B_SHAPE,)
+        per = [_boundary_timing(cfg, args, to_dev, dev, stream, pk) for cfg in cfgs]
+        fl = sum(r["flops"] for r in per)
+        ms = sum(r["ms"] for r in per)
+        value = fl / (ms * 1e-3) / 1e12
+        name = "M sweep 4096..65536 (d=4096, F=16384, P=8, chunks=8)" if args.workload == "msweep" else cfgs[0].name
+        line.update(metric="SP-TP FFN forward TFLOP/s & tokens/s, % of roofline: " + name, value=value,
+                    unit="TFLOP/s", ms_per_step=ms, config={"workload": name, "l2": "inputs larger than L2"},
+                    per_config=[{k: v for k, v in r.items() if k != "flops"} for r in per],
+                    roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                              "frac": value / pk["bf16_sustained"],
+                              "note": "one call of every config, flops over summed time; per-config figures beside"})
     else:
         cfg = synth.DTP_STACK
         inp = synth.dtp_inputs(cfg)
@@ -567,6 +582,37 @@ def run_other(args):
                               "frac": gbs / pk["hbm"], "algorithmic_bytes": by})
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _boundary_timing(cfg, args, to_dev, dev, stream, pk):
+    """Times sptp_ffn_forward on one boundary config (device-resident inputs,
+    about 0.3 s of calls after warm-up)."""
+    import torch
+    import sequence_tensor_transformer_gb300 as st
+    from sequence_tensor_transformer_gb300 import synth
+
+    inp = synth.boundary_inputs(cfg)
+    T = {k: to_dev(v) for k, v in inp.items()}
+    del inp
+    out = torch.empty((cfg.P, cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
+    h = torch.empty_like(T["x"])
+    ws = torch.empty(st.sptp_ffn_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.chunks, st.SPTP_BF16),
+                     dtype=torch.uint8, device=dev)
+
+    def fn():
+        st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.chunks,
+                            cfg.eps, out=out, resid_out=h, workspace=ws)
+    fl = 6.0 * cfg.M * cfg.d * cfg.F
+    est_ms = fl / 1.6e15 * 1e3
+    steps = max(10, int(300.0 / est_ms))
+    ms = timed(fn, steps, max(3, min(args.warmup, 20)), stream)
+    assert st.sptp_read_device_status(ws) == 0
+    value = fl / (ms * 1e-3) / 1e12
+    del T, out, h, ws
+    torch.cuda.empty_cache()
+    return {"workload": cfg.name, "M": cfg.M, "d": cfg.d, "F": cfg.F, "P": cfg.P, "chunks": cfg.chunks,
+            "steps": steps, "ms": ms, "tflops": value, "tokens_per_s": cfg.M / (ms * 1e-3),
+            "frac_sustained": value / pk["bf16_sustained"], "flops": fl}
 
 
 def _fp8_line(args, cfg, to_dev, dev, stream, pk):

@@ -306,19 +306,17 @@ size_t fused_counter_bytes(int M, int P) {
     return (mt + static_cast<size_t>(P) * mt) * sizeof(int);
 }
 
-// Raster band: the GEMMs walk the m-tiles of 4096 rows (or of one sequence
-// chunk, if taller) against each B panel before moving to the next panel, so
-// the band's A tiles stay in L2 while the weights are streamed about M/4096
-// times.  (Measured on the 8192 x 4096 x 14336 boundary, end to end: bands of
-// 1024 / 2048 / 4096 / 8192 rows gave 1589 / 1644 / 1658 / 1602 TFLOP/s.)
+// Raster band: the GEMMs walk the m-tiles of 4096 rows against each B panel
+// before moving to the next panel, so the band's A tiles stay in L2 while the
+// weights are streamed about M/4096 times.  (Measured on the 8192 x 4096 x
+// 14336 boundary, end to end: bands of 1024 / 2048 / 4096 / 8192 rows gave
+// 1589 / 1644 / 1658 / 1602 TFLOP/s; at M=65536 with 8192-row chunks, a band
+// of one chunk gave 1576-1582 and 4096 rows 1599-1601.)  The band does not
+// follow the sequence chunks: in the multi-launch paths every chunk's rows
+// are ready before the GEMM starts.
 constexpr int kBandRows = 4096;
 
-int band_for_chunks(int M, int chunks) {
-    const int chunk_rows = chunks > 0 ? M / chunks : M;
-    const int rows = chunk_rows > kBandRows ? chunk_rows : kBandRows;
-    const int band = rows / kBM;
-    return band < 1 ? 1 : band;
-}
+int raster_band() { return kBandRows / kBM; }
 
 constexpr int SPTP_ERR_UNSUPPORTED = -100;  // internal: fused path not available here
 constexpr int kFirstBandRows = 2048;
@@ -730,7 +728,7 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
     void* sbuf = mptr(workspace, SPTP_WS_HEADER_BYTES + align_up(act));
     int* counters = reinterpret_cast<int*>(
         mptr(workspace, SPTP_WS_HEADER_BYTES + align_up(act) + align_up(static_cast<size_t>(M) * F * es)));
-    const int band = band_for_chunks(M, chunks);
+    const int band = raster_band();
 
     if (dtype == SPTP_BF16 && gemm_variant() == Variant::kFused) {
         rc = fused_forward(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, out, resid_out, y, sbuf,
@@ -854,10 +852,10 @@ int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, co
         const size_t woff = static_cast<size_t>(l) * F * d * es;
         for (int p = 0; p < P; ++p) A[p] = yp(p);
         if ((rc = gateup(A, cptr(W1g, woff), cptr(W1u, woff), M, d, F, P, dtype, sbuf, ws_status(workspace),
-                         band_for_chunks(M, 1), di, s)) != SPTP_OK)
+                         raster_band(), di, s)) != SPTP_OK)
             return rc;
         for (int p = 0; p < P; ++p) outs[p] = o(l, p);
-        if ((rc = down(sbuf, cptr(W2, woff), M, d, F, P, dtype, outs, ws_status(workspace), band_for_chunks(M, 1),
+        if ((rc = down(sbuf, cptr(W2, woff), M, d, F, P, dtype, outs, ws_status(workspace), raster_band(),
                        di, s)) != SPTP_OK)
             return rc;
         (void)f;
@@ -920,7 +918,7 @@ int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u, int M, i
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     const void* A[kMaxGroups];
     for (int g = 0; g < P; ++g) A[g] = y;
-    return gateup(A, W1g, W1u, M, d, F, P, dtype, s_out, ws_status(workspace), band_for_chunks(M, 1), di, s);
+    return gateup(A, W1g, W1u, M, d, F, P, dtype, s_out, ws_status(workspace), raster_band(), di, s);
 }
 
 int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype, void* out,
@@ -945,7 +943,7 @@ int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P,
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     void* outs[kMaxGroups];
     for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * M * d * es);
-    return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), band_for_chunks(M, 1), di, s);
+    return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), raster_band(), di, s);
 }
 
 size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, int dtype) {
@@ -994,7 +992,7 @@ int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma
     int* counters = reinterpret_cast<int*>(mptr(workspace, SPTP_WS_HEADER_BYTES + align_up(act)));
     if (dtype == SPTP_BF16 && attn_fused_selected()) {
         rc = fused_attn_forward(x, partials, gamma, Wqkv, M, d, N, P, chunks, eps, qkv_out, resid_out, y, counters,
-                                ws_status(workspace), band_for_chunks(M, chunks), di, s);
+                                ws_status(workspace), raster_band(), di, s);
         if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
         if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: prologue + GEMM below
     }
@@ -1010,7 +1008,7 @@ int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma
     pp.status = ws_status(workspace);
     pp.wait_limit_ns = kWaitLimitNs;
     if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
-    return colpar_store(y, Wqkv, M, d, N, P, dtype, qkv_out, ws_status(workspace), band_for_chunks(M, chunks), di,
+    return colpar_store(y, Wqkv, M, d, N, P, dtype, qkv_out, ws_status(workspace), raster_band(), di,
                         s);
 }
 
@@ -1140,7 +1138,7 @@ int sptp_ffn_forward_fp8(const void* x, const void* partials, const void* gamma,
     void* sbuf = mptr(workspace, lay.s);
     void* qs = mptr(workspace, lay.qs);
     float* ss = reinterpret_cast<float*>(mptr(workspace, lay.ss));
-    const int band = band_for_chunks(M, chunks);
+    const int band = raster_band();
     const int f = F / P;
 
     // 1-3: partial sum, residual add, RMSNorm -> the bf16 activation y ...
@@ -1234,7 +1232,7 @@ int sptp_gateup_swiglu_e4m3(const void* qy, const float* sy, const void* qW1g, c
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     return gateup_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, M, d, F, P, s_out, ws_status(workspace),
-                       band_for_chunks(M, 1), di, s);
+                       raster_band(), di, s);
 }
 
 int sptp_down_proj_e4m3(const void* qs, const float* ss, const void* qW2, const float* sW2, int M, int d, int F,
@@ -1259,7 +1257,7 @@ int sptp_down_proj_e4m3(const void* qs, const float* ss, const void* qW2, const 
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     void* outs[kMaxGroups];
     for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * M * d * 2);
-    return down_e4m3(qs, ss, qW2, sW2, M, d, F, P, outs, ws_status(workspace), band_for_chunks(M, 1), di, s);
+    return down_e4m3(qs, ss, qW2, sW2, M, d, F, P, outs, ws_status(workspace), raster_band(), di, s);
 }
 
 }  // extern "C"

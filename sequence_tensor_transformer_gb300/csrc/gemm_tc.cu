@@ -10,7 +10,7 @@
 //               one of two TMEM accumulators of 256 fp32 columns
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, SwiGLU or bf16
 //               convert, 16-byte global stores; overlaps the next tile's MMAs
-// Tiles are walked in raster bands of `band` m-tiles (a sequence chunk) so
+// Tiles are walked in raster bands of `band` m-tiles (4096 rows) so
 // that concurrently running CTAs share A and B tiles in L2.
 //
 // The CTA-pair kernel (namespace pair, cta_group::2) is the default: tiles of
