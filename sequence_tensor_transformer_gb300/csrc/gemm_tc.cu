@@ -296,9 +296,9 @@ static_assert(psmem_bytes<kMaxPStages>() <= 227 * 1024, "pipeline does not fit i
 // A stage holds 128-byte K slices of each operand row: 64 bf16 or 128 E4M3
 // elements.  Either way 4 UMMAs of 32 bytes per row consume it.
 template <bool E4M3>
-constexpr int k_elems() { return E4M3 ? 128 : 64; }
+__host__ __device__ constexpr int k_elems() { return E4M3 ? 128 : 64; }
 template <bool E4M3>
-constexpr uint32_t pair_idesc() { return E4M3 ? idesc_e4m3_f32(PBM, PBN) : idesc_bf16_f32(PBM, PBN); }
+__host__ __device__ constexpr uint32_t pair_idesc() { return E4M3 ? idesc_e4m3_f32(PBM, PBN) : idesc_bf16_f32(PBM, PBN); }
 // Epilogue warps EW: 4 (one per TMEM lane quarter) or 8 (two per quarter,
 // each taking half of the tile's columns).
 template <int EW>
