@@ -1,8 +1,8 @@
 // C ABI of libsptp.so: argument validation, workspace layout and the launch
-// sequence of the SP-TP FFN boundary and of the Delayed-TP stack.  Every step
-// of the computation runs in the library's own kernels (prologue.cu,
-// gemm_tc.cu, gemm_simt.cu); this file only checks arguments, lays out the
-// caller's workspace, encodes TMA descriptors and enqueues launches.
+// sequence of every entry point.  Every step of the computation runs in the
+// library's own kernels; this file only checks arguments, lays out the
+// caller's workspace and enqueues launches (the grouped GEMM launches are in
+// launch.cu).
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "launch.h"
 #include "sptp.h"
 #include "sptp_internal.h"
 
@@ -22,7 +23,6 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
-size_t esize(int dtype) { return dtype == SPTP_BF16 ? 2 : 4; }
 
 bool dtype_ok(int dtype) { return dtype == SPTP_BF16 || dtype == SPTP_FP32; }
 
@@ -44,10 +44,6 @@ int check_common(int M, int d, int F, int P, int dtype) {
     return SPTP_OK;
 }
 
-struct DevInfo {
-    int sms = 0;
-    int major = 0, minor = 0;
-};
 
 // Per-device SM count and compute capability, queried once per device.
 int device_info(DevInfo* out) {
@@ -77,197 +73,9 @@ int reset_status(void* ws, cudaStream_t s) {
     return cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), s) == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA; }
 
-const char* cptr(const void* base, size_t off_bytes) { return static_cast<const char*>(base) + off_bytes; }
-char* mptr(void* base, size_t off_bytes) { return static_cast<char*>(base) + off_bytes; }
 
-// ------------------------------------------------------------- GEMM launches
 
-constexpr int kBM = 128, kBNSwiGLU = 128, kBNStore = 256, kBK = 64;
-
-// bf16 execution variant, from the environment variable SPTP_GEMM_VARIANT:
-//   unset / "pair"   prologue + CTA-pair gate/up + CTA-pair down launches
-//   "fused"          the whole boundary in one persistent CTA-pair launch
-//                    (falls back to "pair" where it cannot be launched)
-//   "single"         prologue + single-CTA gate/up + down launches
-// The step-level entry points use "pair" unless "single" is selected.  On the
-// 8192 x 4096 x 14336 boundary the fused launch and "pair" measure level
-// (1670-1675 vs 1668-1669 TFLOP/s); the fused one needs ~7% fewer SM cycles
-// but, under the GPU's power cap, runs at a lower clock.  "pair" stays the
-// default: its kernels can be profiled with ncu, the cooperative launch not.
-enum class Variant { kFused, kPair, kSingle };
-
-Variant gemm_variant() {
-    const char* v = std::getenv("SPTP_GEMM_VARIANT");
-    if (v != nullptr && std::strcmp(v, "single") == 0) return Variant::kSingle;
-    if (v != nullptr && std::strcmp(v, "fused") == 0) return Variant::kFused;
-    return Variant::kPair;
-}
-
-bool use_pair_gemm() { return gemm_variant() != Variant::kSingle; }
-
-// Gate/up + SwiGLU for P groups: s_g = silu(A_g W1g[F_g]^T) * (A_g W1u[F_g]^T).
-int gateup(const void* const* A, const void* W1g, const void* W1u, int M, int d, int F, int P, int dtype,
-           void* s_out, DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
-    const int f = F / P;
-    const size_t es = esize(dtype);
-    if (M == 0) return SPTP_OK;
-    if (dtype == SPTP_BF16) {
-        TcGemmParams p;
-        std::memset(&p, 0, sizeof(p));
-        for (int g = 0; g < P; ++g) {
-            const size_t woff = static_cast<size_t>(g) * f * d * es;
-            if (!encode_map_bf16(&p.mapA[g], A[g], d, M, static_cast<uint64_t>(d) * es, kBK, kBM) ||
-                !encode_map_bf16(&p.mapB0[g], cptr(W1g, woff), d, f, static_cast<uint64_t>(d) * es, kBK,
-                                 kBNSwiGLU) ||
-                !encode_map_bf16(&p.mapB1[g], cptr(W1u, woff), d, f, static_cast<uint64_t>(d) * es, kBK,
-                                 kBNSwiGLU))
-                return SPTP_ERR_CUDA;
-            p.out[g] = mptr(s_out, static_cast<size_t>(g) * M * f * es);
-        }
-        const bool pair = use_pair_gemm();
-        const int bm = pair ? 2 * kBM : kBM;
-        p.ldo = f;
-        p.M = M;
-        p.N = f;
-        p.K = d;
-        p.G = P;
-        p.mt = (M + bm - 1) / bm;
-        p.nt = (f + kBNSwiGLU - 1) / kBNSwiGLU;
-        p.nk = (d + kBK - 1) / kBK;
-        if (pair) band = (band + 1) / 2;
-        p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
-        p.status = st;
-        p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kSwiGLU, di.sms, s)
-                                : launch_tc_gemm(p, Epi::kSwiGLU, di.sms, s));
-    }
-    SimtGemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    for (int g = 0; g < P; ++g) {
-        const size_t woff = static_cast<size_t>(g) * f * d;
-        p.A[g] = static_cast<const float*>(A[g]);
-        p.B0[g] = static_cast<const float*>(W1g) + woff;
-        p.B1[g] = static_cast<const float*>(W1u) + woff;
-        p.C[g] = static_cast<float*>(s_out) + static_cast<size_t>(g) * M * f;
-    }
-    p.lda = d;
-    p.ldb = d;
-    p.ldc = f;
-    p.M = M;
-    p.N = f;
-    p.K = d;
-    p.G = P;
-    return cuda_status(launch_simt_gemm(p, Epi::kSwiGLU, s));
-}
-
-// Down projection for P groups: out_g = s_g W2[:, F_g]^T.
-int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype, void* const* out,
-         DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
-    const int f = F / P;
-    const size_t es = esize(dtype);
-    if (M == 0) return SPTP_OK;
-    if (dtype == SPTP_BF16) {
-        const bool pair = use_pair_gemm();
-        const int bm = pair ? 2 * kBM : kBM;
-        // a CTA pair stages each B tile as two 128-row halves
-        const uint32_t bbox = pair ? kBNStore / 2 : kBNStore;
-        TcGemmParams p;
-        std::memset(&p, 0, sizeof(p));
-        for (int g = 0; g < P; ++g) {
-            if (!encode_map_bf16(&p.mapA[g], cptr(s_in, static_cast<size_t>(g) * M * f * es), f, M,
-                                 static_cast<uint64_t>(f) * es, kBK, kBM) ||
-                !encode_map_bf16(&p.mapB0[g], cptr(W2, static_cast<size_t>(g) * f * es), f, d,
-                                 static_cast<uint64_t>(F) * es, kBK, bbox))
-                return SPTP_ERR_CUDA;
-            p.out[g] = out[g];
-        }
-        p.ldo = d;
-        p.M = M;
-        p.N = d;
-        p.K = f;
-        p.G = P;
-        p.mt = (M + bm - 1) / bm;
-        p.nt = (d + kBNStore - 1) / kBNStore;
-        p.nk = (f + kBK - 1) / kBK;
-        if (pair) band = (band + 1) / 2;
-        p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
-        p.status = st;
-        p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kStore, di.sms, s)
-                                : launch_tc_gemm(p, Epi::kStore, di.sms, s));
-    }
-    SimtGemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    for (int g = 0; g < P; ++g) {
-        p.A[g] = static_cast<const float*>(s_in) + static_cast<size_t>(g) * M * f;
-        p.B0[g] = static_cast<const float*>(W2) + static_cast<size_t>(g) * f;
-        p.B1[g] = nullptr;
-        p.C[g] = static_cast<float*>(out[g]);
-    }
-    p.lda = f;
-    p.ldb = F;
-    p.ldc = d;
-    p.M = M;
-    p.N = d;
-    p.K = f;
-    p.G = P;
-    return cuda_status(launch_simt_gemm(p, Epi::kStore, s));
-}
-
-// Column-parallel projection for P groups with a plain bf16/fp32 store:
-// out_g [M][N/P] = A W[g*N/P .. (g+1)*N/P)^T, W [N][K] row-major.
-int colpar_store(const void* A, const void* W, int M, int K, int N, int P, int dtype, void* out, DeviceStatus* st,
-                 int band, const DevInfo& di, cudaStream_t s) {
-    const int n = N / P;
-    const size_t es = esize(dtype);
-    if (M == 0) return SPTP_OK;
-    if (dtype == SPTP_BF16) {
-        const bool pair = use_pair_gemm();
-        const int bm = pair ? 2 * kBM : kBM;
-        const uint32_t bbox = pair ? kBNStore / 2 : kBNStore;
-        TcGemmParams p;
-        std::memset(&p, 0, sizeof(p));
-        for (int g = 0; g < P; ++g) {
-            if (!encode_map_bf16(&p.mapA[g], A, K, M, static_cast<uint64_t>(K) * es, kBK, kBM) ||
-                !encode_map_bf16(&p.mapB0[g], cptr(W, static_cast<size_t>(g) * n * K * es), K, n,
-                                 static_cast<uint64_t>(K) * es, kBK, bbox))
-                return SPTP_ERR_CUDA;
-            p.out[g] = mptr(out, static_cast<size_t>(g) * M * n * es);
-        }
-        p.ldo = n;
-        p.M = M;
-        p.N = n;
-        p.K = K;
-        p.G = P;
-        p.mt = (M + bm - 1) / bm;
-        p.nt = (n + kBNStore - 1) / kBNStore;
-        p.nk = (K + kBK - 1) / kBK;
-        if (pair) band = (band + 1) / 2;
-        p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
-        p.status = st;
-        p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kStore, di.sms, s)
-                                : launch_tc_gemm(p, Epi::kStore, di.sms, s));
-    }
-    SimtGemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    for (int g = 0; g < P; ++g) {
-        p.A[g] = static_cast<const float*>(A);
-        p.B0[g] = static_cast<const float*>(W) + static_cast<size_t>(g) * n * K;
-        p.B1[g] = nullptr;
-        p.C[g] = static_cast<float*>(out) + static_cast<size_t>(g) * M * n;
-    }
-    p.lda = K;
-    p.ldb = K;
-    p.ldc = n;
-    p.M = M;
-    p.N = n;
-    p.K = K;
-    p.G = P;
-    return cuda_status(launch_simt_gemm(p, Epi::kStore, s));
-}
 
 // Readiness counters of the fused Delayed-TP stack: per module, rows normed
 // and down halves stored per 256-row block; gate/up halves per (shard, block).
@@ -306,24 +114,12 @@ size_t fused_counter_bytes(int M, int P) {
     return (mt + static_cast<size_t>(P) * mt) * sizeof(int);
 }
 
-// Raster band: the GEMMs walk the m-tiles of 4096 rows against each B panel
-// before moving to the next panel, so the band's A tiles stay in L2 while the
-// weights are streamed about M/4096 times.  (Measured on the 8192 x 4096 x
-// 14336 boundary, end to end: bands of 1024 / 2048 / 4096 / 8192 rows gave
-// 1589 / 1644 / 1658 / 1602 TFLOP/s; at M=65536 with 8192-row chunks, a band
-// of one chunk gave 1576-1582 and 4096 rows 1599-1601.)  The band does not
-// follow the sequence chunks: in the multi-launch paths every chunk's rows
-// are ready before the GEMM starts.
-constexpr int kBandRows = 4096;
-
-int raster_band() { return kBandRows / kBM; }
 
 constexpr int SPTP_ERR_UNSUPPORTED = -100;  // internal: fused path not available here
 constexpr int kFirstBandRows = 2048;
 
 // ------------------------------------------------------------ fp8 (E4M3)
 
-constexpr int kBK8 = 128;  // E4M3 elements per 128-byte swizzle row
 
 int check_fp8(int M, int d, int F, int P) {
     const int rc = check_common(M, d, F, P, SPTP_BF16);
@@ -332,71 +128,6 @@ int check_fp8(int M, int d, int F, int P) {
     return SPTP_OK;
 }
 
-// E4M3 gate/up + SwiGLU for P groups on the CTA-pair tcgen05 GEMM.
-int gateup_e4m3(const void* qy, const float* sy, const void* qW1g, const float* sW1g, const void* qW1u,
-                const float* sW1u, int M, int d, int F, int P, void* s_out, DeviceStatus* st, int band,
-                const DevInfo& di, cudaStream_t s) {
-    const int f = F / P;
-    if (M == 0) return SPTP_OK;
-    TcGemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    for (int g = 0; g < P; ++g) {
-        const size_t woff = static_cast<size_t>(g) * f * d;
-        if (!encode_map_u8(&p.mapA[g], qy, d, M, d, kBK8, kBM) ||
-            !encode_map_u8(&p.mapB0[g], cptr(qW1g, woff), d, f, d, kBK8, kBNSwiGLU) ||
-            !encode_map_u8(&p.mapB1[g], cptr(qW1u, woff), d, f, d, kBK8, kBNSwiGLU))
-            return SPTP_ERR_CUDA;
-        p.out[g] = mptr(s_out, static_cast<size_t>(g) * M * f * 2);
-        p.row_scale[g] = sy;
-        p.col_scale0[g] = sW1g + static_cast<size_t>(g) * f;
-        p.col_scale1[g] = sW1u + static_cast<size_t>(g) * f;
-    }
-    p.col_scale_stride = 1;
-    p.ldo = f;
-    p.M = M;
-    p.N = f;
-    p.K = d;
-    p.G = P;
-    p.mt = (M + 2 * kBM - 1) / (2 * kBM);
-    p.nt = (f + kBNSwiGLU - 1) / kBNSwiGLU;
-    p.nk = (d + kBK8 - 1) / kBK8;
-    band = (band + 1) / 2;
-    p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
-    p.status = st;
-    p.wait_limit_ns = kWaitLimitNs;
-    return cuda_status(launch_tc_gemm_pair_e4m3(p, Epi::kSwiGLU, di.sms, s));
-}
-
-// E4M3 down projection for P groups: out_g = (qs_g qW2[:, F_g]^T) ss_g sW2[:, g].
-int down_e4m3(const void* qs, const float* ss, const void* qW2, const float* sW2, int M, int d, int F, int P,
-              void* const* out, DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
-    const int f = F / P;
-    if (M == 0) return SPTP_OK;
-    TcGemmParams p;
-    std::memset(&p, 0, sizeof(p));
-    for (int g = 0; g < P; ++g) {
-        if (!encode_map_u8(&p.mapA[g], cptr(qs, static_cast<size_t>(g) * M * f), f, M, f, kBK8, kBM) ||
-            !encode_map_u8(&p.mapB0[g], cptr(qW2, static_cast<size_t>(g) * f), f, d, F, kBK8, kBNStore / 2))
-            return SPTP_ERR_CUDA;
-        p.out[g] = out[g];
-        p.row_scale[g] = ss + static_cast<size_t>(g) * M;
-        p.col_scale0[g] = sW2 + g;
-    }
-    p.col_scale_stride = P;
-    p.ldo = d;
-    p.M = M;
-    p.N = d;
-    p.K = f;
-    p.G = P;
-    p.mt = (M + 2 * kBM - 1) / (2 * kBM);
-    p.nt = (d + kBNStore - 1) / kBNStore;
-    p.nk = (f + kBK8 - 1) / kBK8;
-    band = (band + 1) / 2;
-    p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
-    p.status = st;
-    p.wait_limit_ns = kWaitLimitNs;
-    return cuda_status(launch_tc_gemm_pair_e4m3(p, Epi::kStore, di.sms, s));
-}
 
 struct Fp8Layout {
     size_t y, qy, sy, s, qs, ss, total;
