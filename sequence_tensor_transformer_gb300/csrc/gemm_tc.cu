@@ -560,12 +560,20 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                         packed[j] = pack_bf16x2(v0, v1);
                     }
                     if (row_ok) {
-                        // the partials are final outputs: evict-first stores
+                        // the outputs are final: evict-first stores
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            if (col + 8 * v < p.N)
-                                __stcs(reinterpret_cast<uint4*>(out + col + 8 * v),
-                                       make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
+                        for (int v = 0; v < 4; ++v) {
+                            const int cv = col + 8 * v;
+                            if (cv >= p.N) continue;
+                            __nv_bfloat16* dst = out + cv;
+                            if (p.split_w > 0) {  // 8-column vectors never straddle blocks (split_w % 8 == 0)
+                                const int blk = cv / p.split_w;
+                                dst = reinterpret_cast<__nv_bfloat16*>(p.out[0]) + blk * p.split_stride +
+                                      static_cast<long long>(row) * p.split_w + (cv - blk * p.split_w);
+                            }
+                            __stcs(reinterpret_cast<uint4*>(dst),
+                                   make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
+                        }
                     }
                 }
             }

@@ -162,6 +162,31 @@ int colpar_store(const void* A, const void* W, int M, int K, int N, int P, int d
         const uint32_t bbox = pair ? kBNStore / 2 : kBNStore;
         TcGemmParams p;
         std::memset(&p, 0, sizeof(p));
+        if (pair && P > 1 && n % kBNStore != 0) {
+            // Every shard reads the same A, so the P shards run as one GEMM
+            // over all N rows of W, each 8-column vector stored to its
+            // shard's [M][N/P] block: no half-empty last tile per shard
+            // (N/P = 1152 fills 4.5 tiles of 256).
+            if (!encode_map_bf16(&p.mapA[0], A, K, M, static_cast<uint64_t>(K) * es, kBK, kBM) ||
+                !encode_map_bf16(&p.mapB0[0], W, K, N, static_cast<uint64_t>(K) * es, kBK, bbox))
+                return SPTP_ERR_CUDA;
+            p.out[0] = out;
+            p.split_w = n;
+            p.split_stride = static_cast<long long>(M) * n;
+            p.ldo = n;
+            p.M = M;
+            p.N = N;
+            p.K = K;
+            p.G = 1;
+            p.mt = (M + bm - 1) / bm;
+            p.nt = (N + kBNStore - 1) / kBNStore;
+            p.nk = (K + kBK - 1) / kBK;
+            band = (band + 1) / 2;
+            p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
+            p.status = st;
+            p.wait_limit_ns = kWaitLimitNs;
+            return cuda_status(launch_tc_gemm_pair(p, Epi::kStore, di.sms, s));
+        }
         for (int g = 0; g < P; ++g) {
             if (!encode_map_bf16(&p.mapA[g], A, K, M, static_cast<uint64_t>(K) * es, kBK, kBM) ||
                 !encode_map_bf16(&p.mapB0[g], cptr(W, static_cast<size_t>(g) * n * K * es), K, n,

@@ -91,6 +91,11 @@ struct TcGemmParams {
     const float* col_scale0[kMaxGroups];  // per output column (B0 row)
     const float* col_scale1[kMaxGroups];  // per SwiGLU up column (B1 row)
     int col_scale_stride;
+    // kStore with split_w > 0: the output columns belong to consecutive
+    // blocks of split_w columns, block j stored at out[0] + j * split_stride
+    // as a [M][split_w] matrix (column-parallel shards computed as one GEMM)
+    int split_w;
+    long long split_stride;
 };
 
 enum class Epi { kSwiGLU, kStore };
