@@ -725,8 +725,9 @@ cudaError_t launch_tc_gemm_pair(const TcGemmParams& p, Epi epi, int num_sms, cud
 
 cudaError_t launch_tc_gemm_pair_e4m3(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s) {
     if (p.G * p.mt * p.nt == 0) return cudaSuccess;
-    // six stages, as for bf16: a seventh measured no faster for either
-    // operand type (8192 x 4096 x 14336: E4M3 step 2824 vs 2824 TFLOP/s)
+    // six stages and four epilogue warps, as for bf16: a seventh stage
+    // measured no faster (8192 x 4096 x 14336: E4M3 step 2824 vs 2824
+    // TFLOP/s), eight epilogue warps slower (E4M3 gate/up 604-608 vs 590 us)
     return epi == Epi::kSwiGLU ? launch_pair_typed<Epi::kSwiGLU, 4, true>(p, num_sms, s)
                                : launch_pair_typed<Epi::kStore, 4, true>(p, num_sms, s);
 }
