@@ -207,6 +207,7 @@ int fused_forward(const void* x, const void* partials, const void* gamma, const 
     p.band0 = first_tiles < 1 ? 1 : (first_tiles > p.band ? p.band : first_tiles);
     p.tiles_gu = P * p.mt * p.nt_gu;
     p.tiles_dn = P * p.mt * p.nt_dn;
+    p.block_rows = P + 1 <= 5 && d <= 4096 ? 1 : 0;
     p.rb_ready = counters;
     p.gu_done = counters + p.mt;
     p.status = st;
@@ -277,6 +278,7 @@ int fused_attn_forward(const void* x, const void* partials, const void* gamma, c
     p.band0 = first_tiles < 1 ? 1 : (first_tiles > p.band ? p.band : first_tiles);
     p.tiles_gu = P * p.mt * p.nt_gu;
     p.tiles_dn = 0;
+    p.block_rows = P + 1 <= 5 && d <= 4096 ? 1 : 0;
     p.rb_ready = counters;
     p.gu_done = counters;  // unused without down tiles
     p.status = st;

@@ -183,6 +183,96 @@ __device__ __forceinline__ void row_h(const FusedParams& p, long long row_off, i
     }
 }
 
+// Block-row prologue (p.block_rows): the PRO_WARPS prologue warps of a CTA take
+// one row together, rows blockIdx.x, blockIdx.x + gridDim.x, ...  Thread t
+// owns the 16-byte column vectors t and t + 32 * PRO_WARPS; the loads of all
+// sources (partials, then x) and both vectors are issued at once, so a row
+// costs one round of loads; h stays in registers (one pass), its sum of
+// squares meets through shared memory at one named barrier per row, and each
+// warp publishes its part of the row (PRO_WARPS increments per row).  The sum
+// of squares is reduced in the standalone prologue's order (one vector per
+// thread, warps of 32 vectors, warp sums added in order), so h and y match
+// it bit for bit: each thread keeps one partial sum per vector.
+constexpr int kBrSrc = 5;  // sources held at once: P + 1 <= 5
+constexpr int kBrVec = 2;  // vectors per thread: d <= 2 * 8 * 32 * PRO_WARPS
+
+__device__ __forceinline__ void prologue_block_rows(const FusedParams& p, int tid, int wp, int lane) {
+    constexpr int NT = 32 * PRO_WARPS;
+    __shared__ float red[2][kBrVec * PRO_WARPS];
+    const int d = p.d;
+    const int nvec = d >> 3;
+    float gm[kBrVec][8];
+#pragma unroll
+    for (int k = 0; k < kBrVec; ++k)
+        if (tid + k * NT < nvec) load8(static_cast<const __nv_bfloat16*>(p.gamma) + (tid + k * NT) * 8, gm[k]);
+    int par = 0;
+    for (long long row = blockIdx.x; row < p.M; row += gridDim.x) {
+        const long long base = row * d;
+        uint4 u[kBrSrc][kBrVec];
+#pragma unroll
+        for (int q = 0; q < kBrSrc; ++q) {
+            if (q > p.P) break;
+            const __nv_bfloat16* src = q < p.P ? static_cast<const __nv_bfloat16*>(p.partials[q])
+                                               : static_cast<const __nv_bfloat16*>(p.x);
+#pragma unroll
+            for (int k = 0; k < kBrVec; ++k)
+                if (tid + k * NT < nvec)
+                    u[q][k] = __ldg(reinterpret_cast<const uint4*>(src + base + (tid + k * NT) * 8));
+        }
+        // partials in order, then x (one IEEE addition: h + x == x + h)
+        float h[kBrVec][8];
+        float ssk[kBrVec];
+#pragma unroll
+        for (int k = 0; k < kBrVec; ++k) {
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) h[k][e] = 0.f;
+#pragma unroll
+            for (int q = 0; q < kBrSrc; ++q) {
+                if (q > p.P || tid + k * NT >= nvec) break;
+                const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u[q][k]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f2 = __bfloat1622float2(h2[i]);
+                    h[k][2 * i] += f2.x;
+                    h[k][2 * i + 1] += f2.y;
+                }
+            }
+            if (tid + k * NT < nvec)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(h[k][e], h[k][e], ss);
+            ssk[k] = ss;
+        }
+        // vector k * NT + t belongs to "warp" k * PRO_WARPS + wp of 32 vectors
+#pragma unroll
+        for (int k = 0; k < kBrVec; ++k) {
+            const float ws = warp_sum(ssk[k]);
+            if (lane == 0) red[par][k * PRO_WARPS + wp] = ws;
+        }
+        named_barrier_sync<2, NT>();
+        float ss = 0.f;
+#pragma unroll
+        for (int w = 0; w < kBrVec * PRO_WARPS; ++w) ss += red[par][w];
+        par ^= 1;
+        const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
+#pragma unroll
+        for (int k = 0; k < kBrVec; ++k) {
+            const int col = (tid + k * NT) * 8;
+            if (col >= d) continue;
+            if (p.h_out != nullptr)
+                __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.h_out) + base + col), pack8(h[k]));
+            float yv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) yv[e] = (h[k][e] * gm[k][e]) * inv;
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + base + col) = pack8(yv);
+        }
+        // make this warp's part of y visible to the TMA loads of other CTAs
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) red_release_add(&p.rb_ready[row >> 8], 1);
+    }
+}
+
 __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid_constant__ FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -234,8 +324,11 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
     const int pair_id = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
 
-    if (warp >= 6) {
-        // ------------------------------------------------ prologue rows
+    if (warp >= 6 && p.block_rows) {
+        // ------------------------------------------------ prologue rows, one per CTA at a time
+        prologue_block_rows(p, threadIdx.x - 6 * 32, warp - 6, lane);
+    } else if (warp >= 6) {
+        // ------------------------------------------------ prologue rows, one per warp
         const int W = gridDim.x * PRO_WARPS;
         const int d = p.d;
         for (long long row = static_cast<long long>(blockIdx.x) * PRO_WARPS + (warp - 6); row < p.M; row += W) {
@@ -267,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                             __stcs(reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.h_out) + base + col),
                                    pack8(h[v]));
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) gm[e] = h[v][e] * inv * gm[e];
+                        for (int e = 0; e < 8; ++e) gm[e] = (h[v][e] * gm[e]) * inv;
                         *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.y) + base + col) = pack8(gm);
                     }
                 }
@@ -289,7 +382,8 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             const Tile tl = decode(p, t);
             // dependency of this tile's A operand
             if (!tl.down) {
-                const int need = min(PBM, p.M - tl.m * PBM);
+                // a row counts once per publishing warp
+                const int need = min(PBM, p.M - tl.m * PBM) * (p.block_rows ? PRO_WARPS : 1);
                 ok = flag_wait_geq(&p.rb_ready[tl.m], need, wc, kWhereFusedRows, t);
             } else {
                 ok = flag_wait_geq(&p.gu_done[tl.g * p.mt + tl.m], 2 * p.nt_gu, wc, kWhereFusedGateUp, t);

@@ -148,6 +148,10 @@ struct FusedParams {
     // a column-parallel store GEMM (B = mapW1g[g], shard g's Wqkv rows [f][d];
     // output s_out[g] [M][f]) and there is no down phase (tiles_dn == 0).
     int qkv;
+    // block_rows != 0: the CTA's prologue warps take one row together (needs
+    // P + 1 <= 5 sources and d <= 4096); each of them publishes its part, so a
+    // row adds PRO_WARPS to rb_ready
+    int block_rows;
     int* rb_ready;                     // [mt] prologue rows done per 256-row block
     int* gu_done;                      // [P][mt] gate/up tile halves stored
     DeviceStatus* status;

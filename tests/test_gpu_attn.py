@@ -88,3 +88,20 @@ def test_attn_out_projection_qwen2_7b_shape_sampled_rows():
     got = host_f64(out[:, rows])
     for p in range(cfg.P):
         assert rel_err(got[p], ref[p]) <= TOL["bf16"], p
+
+
+def test_fused_qkv_boundary_equals_two_launch_path_bitwise(monkeypatch):
+    """The fused attention-side boundary and prologue + QKV GEMM compute the
+    same y and the same tiles: identical outputs."""
+    cfg = synth.AttnConfig("bitwise", 1024, 3584, 4 * 1152, 4 * 896, 4, 8, "bf16")
+    inp = synth.attn_inputs(cfg)
+    T = {k: dev_tensor(inp[k], "bf16") for k in ("x", "partials", "gamma", "Wqkv")}
+    res = {}
+    for variant in ("two_launch", "fused"):
+        if variant == "fused":
+            monkeypatch.setenv("SPTP_ATTN_VARIANT", "fused")
+        qkv, h = st.sptp_attn_qkv_forward(T["x"], T["partials"], T["gamma"], T["Wqkv"], cfg.P, cfg.chunks, cfg.eps)
+        res[variant] = (qkv.clone(), h.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(res["fused"][1], res["two_launch"][1])
+    assert torch.equal(res["fused"][0], res["two_launch"][0])

@@ -300,3 +300,21 @@ def test_bounded_wait_reports_timeout_without_hanging():
     # the context is still usable afterwards
     cfg = synth.TINY_FP32
     check(*run_boundary(cfg), "fp32")
+
+
+@pytest.mark.parametrize("M,d,F,P,C", [(1024, 4096, 2 * 1024, 2, 2), (512, 3584, 4 * 512, 4, 4), (300, 1000, 3 * 128, 3, 3)])
+def test_fused_boundary_equals_three_launch_path_bitwise(M, d, F, P, C, monkeypatch):
+    """With up to 5 sources and d <= 4096 the fused launch's prologue (one
+    row per CTA) reduces in the standalone prologue's order and every GEMM
+    tile runs the same UMMAs, so the outputs match bit for bit."""
+    cfg = case(M, d, F, P, C, "bf16")
+    T = {k: dev_tensor(v, "bf16") for k, v in synth.boundary_inputs(cfg).items()}
+    res = {}
+    for variant in ("pair", "fused"):
+        monkeypatch.setenv("SPTP_GEMM_VARIANT", variant)
+        out, h = st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P, C,
+                                     cfg.eps)
+        res[variant] = (out.clone(), h.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(res["fused"][1], res["pair"][1])
+    assert torch.equal(res["fused"][0], res["pair"][0])
