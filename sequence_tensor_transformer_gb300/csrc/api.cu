@@ -151,7 +151,7 @@ Fp8Layout fp8_layout(int M, int d, int F, int P) {
 int fused_forward(const void* x, const void* partials, const void* gamma, const void* W1g, const void* W1u,
                   const void* W2, int M, int d, int F, int P, int chunks, float eps, void* out, void* resid_out,
                   void* y, void* sbuf, int* counters, DeviceStatus* st, int band, const DevInfo& di,
-                  cudaStream_t s) {
+                  cudaStream_t s, bool pre_normed = false) {
     static bool unavailable[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -208,6 +208,7 @@ int fused_forward(const void* x, const void* partials, const void* gamma, const 
     p.tiles_gu = P * p.mt * p.nt_gu;
     p.tiles_dn = P * p.mt * p.nt_dn;
     p.block_rows = P + 1 <= 5 && d <= 4096 ? 1 : 0;
+    p.pre_normed = pre_normed ? 1 : 0;
     p.rb_ready = counters;
     p.gu_done = counters + p.mt;
     p.status = st;
@@ -483,6 +484,14 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
     pp.status = ws_status(workspace);
     pp.wait_limit_ns = kWaitLimitNs;
     if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
+
+    if (dtype == SPTP_BF16 && gemm_variant() == Variant::kChain) {
+        // 4-7 as one persistent launch: gate/up and down tiles in one sequence
+        rc = fused_forward(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, out, resid_out, y, sbuf,
+                           counters, ws_status(workspace), band, di, s, true);
+        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
+        if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: the two GEMM launches below
+    }
 
     // 4-6: chunked gather (identity) + column-parallel gate/up + SwiGLU,
     // tiles walked chunk by chunk

@@ -324,7 +324,9 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
     const int pair_id = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
 
-    if (warp >= 6 && p.block_rows) {
+    if (warp >= 6 && p.pre_normed) {
+        // y is already written: nothing for the prologue warps to do
+    } else if (warp >= 6 && p.block_rows) {
         // ------------------------------------------------ prologue rows, one per CTA at a time
         prologue_block_rows(p, threadIdx.x - 6 * 32, warp - 6, lane);
     } else if (warp >= 6) {
@@ -382,9 +384,11 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             const Tile tl = decode(p, t);
             // dependency of this tile's A operand
             if (!tl.down) {
-                // a row counts once per publishing warp
-                const int need = min(PBM, p.M - tl.m * PBM) * (p.block_rows ? PRO_WARPS : 1);
-                ok = flag_wait_geq(&p.rb_ready[tl.m], need, wc, kWhereFusedRows, t);
+                if (!p.pre_normed) {
+                    // a row counts once per publishing warp
+                    const int need = min(PBM, p.M - tl.m * PBM) * (p.block_rows ? PRO_WARPS : 1);
+                    ok = flag_wait_geq(&p.rb_ready[tl.m], need, wc, kWhereFusedRows, t);
+                }
             } else {
                 ok = flag_wait_geq(&p.gu_done[tl.g * p.mt + tl.m], 2 * p.nt_gu, wc, kWhereFusedGateUp, t);
             }

@@ -13,6 +13,9 @@ namespace sptp {
 //   unset / "pair"   prologue + CTA-pair gate/up + CTA-pair down launches
 //   "fused"          the whole boundary in one persistent CTA-pair launch
 //                    (falls back to "pair" where it cannot be launched)
+//   "chain"          prologue launch + one persistent CTA-pair launch running
+//                    the gate/up tiles and then the down tiles (falls back to
+//                    "pair" where it cannot be launched)
 //   "single"         prologue + single-CTA gate/up + down launches
 // The step-level entry points use "pair" unless "single" is selected.  On the
 // 8192 x 4096 x 14336 boundary the fused launch and "pair" measure level
@@ -23,6 +26,7 @@ Variant gemm_variant() {
     const char* v = std::getenv("SPTP_GEMM_VARIANT");
     if (v != nullptr && std::strcmp(v, "single") == 0) return Variant::kSingle;
     if (v != nullptr && std::strcmp(v, "fused") == 0) return Variant::kFused;
+    if (v != nullptr && std::strcmp(v, "chain") == 0) return Variant::kChain;
     return Variant::kPair;
 }
 

@@ -26,7 +26,7 @@ inline const char* cptr(const void* base, size_t off_bytes) { return static_cast
 inline char* mptr(void* base, size_t off_bytes) { return static_cast<char*>(base) + off_bytes; }
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA; }
 
-enum class Variant { kFused, kPair, kSingle };
+enum class Variant { kFused, kChain, kPair, kSingle };
 Variant gemm_variant();
 bool use_pair_gemm();
 

@@ -152,6 +152,9 @@ struct FusedParams {
     // P + 1 <= 5 sources and d <= 4096); each of them publishes its part, so a
     // row adds PRO_WARPS to rb_ready
     int block_rows;
+    // pre_normed != 0: y was written by a preceding prologue launch (stream
+    // order); the prologue warps idle and gate/up tiles do not wait for rows
+    int pre_normed;
     int* rb_ready;                     // [mt] prologue rows done per 256-row block
     int* gu_done;                      // [P][mt] gate/up tile halves stored
     DeviceStatus* status;

@@ -31,12 +31,13 @@ def _lib():
     torch.cuda.set_device(0)
 
 
-@pytest.fixture(params=["fused", "pair", "single"])
+@pytest.fixture(params=["fused", "chain", "pair", "single"])
 def gemm_variant(request, monkeypatch):
     """Runs a test with each bf16 execution variant: the fused persistent
-    boundary (default), and the three-launch paths on CTA-pair or single-CTA
-    tcgen05 GEMMs (the step-level entry points use the CTA-pair GEMMs unless
-    "single" is selected)."""
+    boundary, the prologue followed by one persistent launch of all GEMM
+    tiles ("chain"), and the three-launch paths on CTA-pair (the default) or
+    single-CTA tcgen05 GEMMs (the step-level entry points use the CTA-pair
+    GEMMs unless "single" is selected)."""
     monkeypatch.setenv("SPTP_GEMM_VARIANT", request.param)
     return request.param
 
