@@ -537,8 +537,9 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     }
                 }
             }
+            // reads complete and fenced; outputs are published separately below
             tc_fence_before();
-            mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+            mbar_arrive_cluster_relaxed(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
             if (!tl.down && !p.qkv) {
                 // this CTA's 128 rows of the s tile are stored: publish them
                 // to the down tiles' TMA loads

@@ -523,8 +523,9 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
                     }
                 }
             }
+            // reads complete and fenced; outputs are published separately below
             tc_fence_before();
-            mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+            mbar_arrive_cluster_relaxed(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
             // this CTA's half of the tile is stored: publish it (s to the down
             // tiles' TMA loads, the partial to the next steps' prologue rows)
             fence_proxy_async_global();

@@ -577,8 +577,13 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                     }
                 }
             }
+            // The accumulator's reads are complete (tcgen05.wait::ld) and
+            // ordered before this signal by the fence; nothing else hangs on
+            // it, so it need not wait for this thread's output stores to
+            // drain, as a release arrive would (with 14-k-block tiles that
+            // drain cost 9 % of the attention out-projection: 333 vs 305 us).
             tc_fence_before();
-            mbar_arrive_cluster(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+            mbar_arrive_cluster_relaxed(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
         }
     }
 

@@ -274,6 +274,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// The same arrive without release semantics: it orders nothing of this
+// thread's earlier memory writes (for signals that only order tcgen05 work,
+// made complete beforehand by tcgen05.wait and tcgen05.fence).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 2-D tiled TMA load into this CTA's shared memory whose completion bytes are
 // counted on an mbarrier of either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t mbar_cluster,
