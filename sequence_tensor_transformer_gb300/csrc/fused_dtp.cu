@@ -527,8 +527,9 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
             tc_fence_before();
             mbar_arrive_cluster_relaxed(acc_empty0 + static_cast<uint32_t>(acc * sizeof(uint64_t)));
             // this CTA's half of the tile is stored: publish it (s to the down
-            // tiles' TMA loads, the partial to the next steps' prologue rows)
-            fence_proxy_async_global();
+            // tiles' TMA loads, which needs the proxy fence; the partial to the
+            // next steps' prologue rows, plain loads: release/acquire suffices)
+            if (!tl.down) fence_proxy_async_global();
             named_barrier_sync<1, 32 * EPI_WARPS>();
             if (warp == 2 && lane == 0) {
                 if (!tl.down)
