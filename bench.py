@@ -362,6 +362,24 @@ def run_ours(args):
         iso.append((a, b))
     torch.cuda.synchronize()
     ms_pro_iso = statistics.median(a.elapsed_time(b) for a, b in iso[3:])
+    # single calls, each timed alone: with L2 as the previous call left it, and
+    # after reading 512 MB (L2 clean; the flush itself is not timed)
+    calls = {"warm": [], "l2_flushed": []}
+    for kind, lst in calls.items():
+        for i in range(23):
+            if kind == "l2_flushed":
+                flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            lst.append((a, b))
+    torch.cuda.synchronize()
+    per_call = {}
+    for kind, lst in calls.items():
+        t = [a.elapsed_time(b) for a, b in lst[3:]]
+        per_call[kind] = {"calls": len(t), "median_ms": statistics.median(t), "min_ms": min(t),
+                          "median_tflops": flops_per_step(cfg) / (statistics.median(t) * 1e-3) / 1e12}
     del flush
     pk = peaks()
     gate_fl = 4.0 * M * d * F
@@ -385,7 +403,7 @@ def run_ours(args):
     for k in kernels.values():
         k["frac"] = k["achieved"] / k["peak"]
     top = kernels["gateup_swiglu"]
-    roofline = {"bound": "tensor", "kernel": "tc_gemm_kernel<SwiGLU> (gate/up + SwiGLU)",
+    roofline = {"bound": "tensor", "kernel": "tc_gemm_pair_kernel<SwiGLU> (gate/up + SwiGLU)",
                 "achieved": top["achieved"], "peak": top["peak"], "unit": "TFLOP/s", "frac": top["frac"],
                 "traffic": top["traffic"],
                 "peak_kind": f"bf16_tflops_sustained ({pk['source']}); burst frac "
@@ -464,7 +482,7 @@ def run_ours(args):
                 "frac_of_bf16_peak": {"sustained": value / world / pk["bf16_sustained"],
                                       "burst": value / world / pk["bf16_burst"]},
                 "config": config_json(cfg, {"parallelism": f"replicas x{world} (P={P} shards emulated per GPU)"}),
-                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "kernels": kernels, "per_call": per_call, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": 3 * args.steps, "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -553,8 +571,16 @@ def run_other(args):
         ms = sum(r["ms"] for r in per)
         value = fl / (ms * 1e-3) / 1e12
         name = "M sweep 4096..65536 (d=4096, F=16384, P=8, chunks=8)" if args.workload == "msweep" else cfgs[0].name
+        # the oracle on a fixed 512-row sample (per-row work is the same at every M of the sweep)
+        ccfg = cfgs[0]
+        csec = oracle_rate(ccfg, min(512, ccfg.M))
+        rows = min(512, ccfg.M)
+        cpu = {"value": 6.0 * rows * ccfg.d * ccfg.F / csec / 1e12, "unit": "TFLOP/s", "tokens_per_s": rows / csec,
+               "cores": cores(), "kind": "oracle",
+               "sample": f"first {rows} token rows of {ccfg.name}, float64 numpy oracle, {csec:.2f} s"}
         line.update(metric="SP-TP FFN forward TFLOP/s & tokens/s, % of roofline: " + name, value=value,
                     unit="TFLOP/s", ms_per_step=ms, config={"workload": name, "l2": "inputs larger than L2"},
+                    cpu_baseline=cpu,
                     per_config=[{k: v for k, v in r.items() if k != "flops"} for r in per],
                     roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                               "frac": value / pk["bf16_sustained"],
