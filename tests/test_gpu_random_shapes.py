@@ -1,0 +1,125 @@
+"""GPU parity on seeded random shapes: every entry point against the oracle on
+irregular sizes (M not a tile multiple, d and F/P off the 64/128/256 tile
+grid, P from 1 to 8, several chunk counts), to exercise the tile edges, the
+zero-filled TMA boxes and the ragged tails of every kernel."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_tensor_transformer_gb300 as st
+from oracle import fp8_oracle as f8
+from sequence_tensor_transformer_gb300 import synth
+
+from helpers import TOL, dev_tensor, host_f64, rel_err, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    st.load_library()
+    torch.cuda.set_device(0)
+
+
+def shapes(seed, n, mult=8):
+    """n boundary shapes (M, d, F, P, C) with d % mult == 0 and (F/P) % mult == 0."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        P = int(rng.integers(1, 9))
+        C = P * int(rng.integers(1, 4))
+        M = C * int(rng.integers(1, 700 // C + 1))
+        d = mult * int(rng.integers(2, 1536 // mult + 1))
+        F = P * mult * int(rng.integers(1, 640 // mult + 1))
+        out.append((M, d, F, P, C))
+    return out
+
+
+def check_boundary(cfg, out, h, ref, href, tol):
+    got = host_f64(out)
+    for p in range(cfg.P):
+        assert rel_err(got[p], ref[p]) <= tol, (cfg.name, p, rel_err(got[p], ref[p]))
+    assert rel_err(host_f64(h), href) <= tol, cfg.name
+
+
+@pytest.mark.parametrize("variant", ["pair", "chain", "fused"])
+@pytest.mark.parametrize("shape", shapes(101, 8))
+def test_random_boundary_bf16(shape, variant, monkeypatch):
+    monkeypatch.setenv("SPTP_GEMM_VARIANT", variant)
+    M, d, F, P, C = shape
+    cfg = synth.BoundaryConfig(f"r_{M}_{d}_{F}_{P}_{C}", M, d, F, P, C, "bf16", True, seed=M + d)
+    inp = synth.boundary_inputs(cfg)
+    T = {k: dev_tensor(v, "bf16") for k, v in inp.items()}
+    out, h = st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P, C, cfg.eps)
+    torch.cuda.synchronize()
+    f64 = {k: to_f64(v, "bf16") for k, v in inp.items()}
+    ref, href = oracle.sptp_ffn_forward(f64["x"], f64["partials"], f64["gamma"], f64["W1g"], f64["W1u"], f64["W2"],
+                                        P, C, cfg.eps)
+    check_boundary(cfg, out, h, ref, href, TOL["bf16"])
+
+
+@pytest.mark.parametrize("shape", shapes(202, 8, mult=16))
+def test_random_boundary_fp8(shape):
+    M, d, F, P, C = shape
+    cfg = synth.BoundaryConfig(f"r8_{M}_{d}_{F}_{P}_{C}", M, d, F, P, C, "bf16", True, seed=M + 3 * d)
+    inp = synth.boundary_inputs(cfg)
+    T = {k: dev_tensor(v, "bf16") for k, v in inp.items()}
+    qw = st.quantize_ffn_weights_e4m3(T["W1g"], T["W1u"], T["W2"], P)
+    out, h = st.sptp_ffn_forward_fp8(T["x"], T["partials"], T["gamma"], qw, P, C, cfg.eps)
+    torch.cuda.synchronize()
+    f64 = {k: to_f64(v, "bf16") for k, v in inp.items()}
+    ref, href = f8.sptp_ffn_forward_fp8(f64["x"], f64["partials"], f64["gamma"], f64["W1g"], f64["W1u"],
+                                        f64["W2"], P, C, cfg.eps)
+    check_boundary(cfg, out, h, ref, href, TOL["bf16"])
+
+
+@pytest.mark.parametrize("variant", ["fused", "layers"])
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_random_dtp_stack(seed, variant, monkeypatch):
+    monkeypatch.setenv("SPTP_DTP_VARIANT", variant)
+    rng = np.random.default_rng(300 + seed)
+    P = int(rng.integers(1, 5))
+    L = int(rng.integers(1, 5))
+    delta = int(rng.integers(0, 4))
+    M = int(rng.integers(1, 600))
+    d = 8 * int(rng.integers(2, 129))
+    F = P * 8 * int(rng.integers(1, 49))
+    flush = int(rng.integers(0, 2))
+    cfg = synth.DTPConfig(f"rd_{seed}", M, d, F, P, L, delta, "bf16")
+    inp = synth.dtp_inputs(cfg, independent_streams=bool(seed % 2))
+    T = {k: dev_tensor(v, "bf16") for k, v in inp.items()}
+    st.dtp_ffn_stack_forward(T["x_shards"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P, L, delta, flush, cfg.eps)
+    torch.cuda.synchronize()
+    f64 = {k: to_f64(v, "bf16") for k, v in inp.items()}
+    ref = oracle.dtp_ffn_stack_forward(f64["x_shards"], f64["gamma"], f64["W1g"], f64["W1u"], f64["W2"], P, L, delta,
+                                       bool(flush), cfg.eps)
+    got = host_f64(T["x_shards"])
+    for p in range(P):
+        assert rel_err(got[p], ref[p]) <= TOL["bf16"], (cfg, p)
+
+
+@pytest.mark.parametrize("variant", ["two_launch", "fused"])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_random_attention_boundary(seed, variant, monkeypatch):
+    if variant == "fused":
+        monkeypatch.setenv("SPTP_ATTN_VARIANT", "fused")
+    rng = np.random.default_rng(400 + seed)
+    P = int(rng.integers(1, 9))
+    C = P * int(rng.integers(1, 3))
+    M = C * int(rng.integers(1, 600 // C + 1))
+    d = 8 * int(rng.integers(2, 193))
+    N = P * 8 * int(rng.integers(1, 97))
+    cfg = synth.AttnConfig(f"ra_{seed}", M, d, N, N, P, C, "bf16")
+    inp = synth.attn_inputs(cfg)
+    T = {k: dev_tensor(inp[k], "bf16") for k in ("x", "partials", "gamma", "Wqkv")}
+    qkv, h = st.sptp_attn_qkv_forward(T["x"], T["partials"], T["gamma"], T["Wqkv"], P, C, cfg.eps)
+    torch.cuda.synchronize()
+    ref, href = oracle.attn_qkv_boundary(to_f64(inp["x"], "bf16"), to_f64(inp["partials"], "bf16"),
+                                         to_f64(inp["gamma"], "bf16"), to_f64(inp["Wqkv"], "bf16"), P, C, cfg.eps)
+    got = host_f64(qkv)
+    for p in range(P):
+        assert rel_err(got[p], ref[p]) <= TOL["bf16"], (cfg, p)
+    assert rel_err(host_f64(h), href) <= TOL["bf16"]
