@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 
 #include "sptp_ptx.cuh"
+#include "store_staged.cuh"
 
 namespace sptp {
 
@@ -45,9 +46,11 @@ constexpr int A_BYTES = 128 * BK * 2;
 constexpr int B_BYTES = 128 * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 4;
+// pipeline stages, barriers, then one output staging buffer per epilogue warp
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + EPI_WARPS * kOutWarpBytes;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr int PRO_WARPS = 6;
 constexpr int PRO_WARP0 = 2 + EPI_WARPS;
 constexpr int THREADS = 32 * (2 + EPI_WARPS + PRO_WARPS);
@@ -263,6 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
     uint8_t* a_tiles = smem;
     uint8_t* b_tiles = smem + STAGES * A_BYTES;
     Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* out_stage = smem + STAGES * STAGE_BYTES + BAR_BYTES;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -461,7 +465,6 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
         // epilogue warps the tile's columns are split between them
         constexpr int kSplits = EPI_WARPS / 4;
         const int split = (warp - 2) / 4;
-        const int row_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
         const long long act = static_cast<long long>(p.M) * p.d;
         int local = 0;
         for (int t = pair_id; t < total; t += npairs, ++local) {
@@ -471,56 +474,51 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
             if (named_barrier_any<1, 32 * EPI_WARPS>(!ok)) break;
             tc_fence_after();
             const Tile tl = decode(p, t);
-            const int row = tl.m * PBM + row_in_tile;
-            const bool row_ok = row < p.M;
+            const int row0 = tl.m * PBM + static_cast<int>(rank) * 128 + quarter * 32;  // the warp's first row
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
+            uint8_t* wbuf = out_stage + (warp - 2) * kOutWarpBytes;
             if (!tl.down) {
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.s) +
-                                     (static_cast<long long>(tl.p) * p.M + row) * p.f;
+                // s [M][f] of shard p, in blocks of 64 SwiGLU columns
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.s) + static_cast<long long>(tl.p) * p.M * p.f;
 #pragma unroll 1
-                for (int c = split * (PBN / 2 / kSplits); c < (split + 1) * (PBN / 2 / kSplits); c += 16) {
-                    uint32_t gv[16], uv[16];
-                    tmem_ld_16cols(taddr + c, gv);
-                    tmem_ld_16cols(taddr + PBN / 2 + c, uv);
-                    tmem_ld_wait();
-                    uint32_t packed[8];
+                for (int c0 = split * (PBN / 2 / kSplits); c0 < (split + 1) * (PBN / 2 / kSplits); c0 += 64) {
+                    uint32_t packed[32];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
-                        const float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
-                        packed[j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
-                    }
-                    const int col = tl.n * (PBN / 2) + c;
-                    if (row_ok) {
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t gv[16], uv[16];
+                        tmem_ld_16cols(taddr + c0 + 16 * q, gv);
+                        tmem_ld_16cols(taddr + PBN / 2 + c0 + 16 * q, uv);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int v = 0; v < 2; ++v)
-                            if (col + 8 * v < p.f)
-                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
-                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                        for (int j = 0; j < 8; ++j) {
+                            const float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
+                            const float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
+                            packed[8 * q + j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
+                        }
                     }
+                    store_block_staged<false>(wbuf, packed, lane, out, p.f, nullptr, 0, 0, row0, p.M,
+                                              tl.n * (PBN / 2) + c0, p.f);
                 }
             } else {
+                // the partial [M][d] in ring slot l mod S, shard p, in blocks of 64 columns
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.ring) +
-                                     (static_cast<long long>(tl.l % p.S) * p.P + tl.p) * act +
-                                     static_cast<long long>(row) * p.d;
+                                     (static_cast<long long>(tl.l % p.S) * p.P + tl.p) * act;
 #pragma unroll 1
-                for (int c = split * (PBN / kSplits); c < (split + 1) * (PBN / kSplits); c += 16) {
-                    uint32_t v16[16];
-                    tmem_ld_16cols(taddr + c, v16);
-                    tmem_ld_wait();
-                    uint32_t packed[8];
+                for (int c0 = split * (PBN / kSplits); c0 < (split + 1) * (PBN / kSplits); c0 += 64) {
+                    uint32_t packed[32];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        packed[j] = pack_bf16x2(__uint_as_float(v16[2 * j]), __uint_as_float(v16[2 * j + 1]));
-                    const int col = tl.n * PBN + c;
-                    if (row_ok) {
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t v16[16];
+                        tmem_ld_16cols(taddr + c0 + 16 * q, v16);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int v = 0; v < 2; ++v)
-                            if (col + 8 * v < p.d)
-                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
-                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                        for (int j = 0; j < 8; ++j)
+                            packed[8 * q + j] =
+                                pack_bf16x2(__uint_as_float(v16[2 * j]), __uint_as_float(v16[2 * j + 1]));
                     }
+                    store_block_staged<false>(wbuf, packed, lane, out, p.d, nullptr, 0, 0, row0, p.M,
+                                              tl.n * PBN + c0, p.d);
                 }
             }
             // reads complete and fenced; outputs are published separately below

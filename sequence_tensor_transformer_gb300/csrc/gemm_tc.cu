@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include "sptp_ptx.cuh"
+#include "store_staged.cuh"
 
 namespace sptp {
 
@@ -286,13 +287,17 @@ namespace pair {
 
 constexpr int PBM = 256;                     // tile rows (128 per CTA)
 constexpr int PBN = 256;                     // UMMA N
-constexpr int kMaxPStages = 7;              // 7 x 32 KiB + barriers still fits in 227 KiB
+constexpr int kMaxPStages = 6;
 constexpr int A_BYTES = 128 * BK * 2;        // 16 KiB
 constexpr int B_BYTES = 128 * BK * 2;        // 16 KiB (half of the B tile)
 constexpr int PSTAGE_BYTES = A_BYTES + B_BYTES;
-template <int ST>
-constexpr int psmem_bytes() { return 1024 + ST * PSTAGE_BYTES + BAR_BYTES; }
-static_assert(psmem_bytes<kMaxPStages>() <= 227 * 1024, "pipeline does not fit in shared memory");
+// The plain epilogue stages its output blocks (store_staged.cuh): one
+// kOutWarpBytes buffer per epilogue warp after the barrier block.
+template <Epi EPI, int ST, int EW>
+constexpr int psmem_bytes() {
+    return 1024 + ST * PSTAGE_BYTES + BAR_BYTES + (EPI == Epi::kStore ? EW * kOutWarpBytes : 0);
+}
+static_assert(psmem_bytes<Epi::kStore, kMaxPStages, 4>() <= 227 * 1024, "pipeline does not fit in shared memory");
 // A stage holds 128-byte K slices of each operand row: 64 bf16 or 128 E4M3
 // elements.  Either way 4 UMMAs of 32 bytes per row consume it.
 template <bool E4M3>
@@ -351,6 +356,7 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
     uint8_t* a_tiles = smem;
     uint8_t* b_tiles = smem + PSTAGES * A_BYTES;
     Bars* bars = reinterpret_cast<Bars*>(smem + PSTAGES * PSTAGE_BYTES);
+    uint8_t* out_stage = smem + PSTAGES * PSTAGE_BYTES + BAR_BYTES;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -491,7 +497,6 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
         const uint32_t acc_empty0 = mapa_shared(smem_u32(&bars->acc_empty[0]), 0);
         const int quarter = warp & 3;
         const int half = (warp - 2) / 4;
-        const int row_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
         int local = 0;
         for (int t = pair_id; t < total; t += npairs, ++local) {
             const int acc = local & 1;
@@ -501,15 +506,20 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
             tc_fence_after();
             int g, m, n;
             decode_tile(p, t, g, m, n);
-            const int row = m * PBM + row_in_tile;
+            const int row0 = m * PBM + static_cast<int>(rank) * 128 + quarter * 32;  // the warp's first row
+            const int row = row0 + lane;
             const bool row_ok = row < p.M;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[g]) + static_cast<long long>(row) * p.ldo;
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[g]);
             // E4M3: the token row's scale (power of two; rows past M read none)
             float rs = 1.0f;
             if constexpr (E4M3) rs = row_ok ? __ldg(p.row_scale[g] + row) : 0.0f;
             if (EPI == Epi::kSwiGLU) {
+                // each lane stores its own row: 64 bytes per 32 columns (the
+                // stores are half the plain epilogue's per tile, and gate/up
+                // K is long, so staging them measured no faster)
+                __nv_bfloat16* orow = out + static_cast<long long>(row) * p.ldo;
 #pragma unroll 1
                 for (int c = half * (PBN / 2 / kSplits); c < (half + 1) * (PBN / 2 / kSplits); c += 32) {
                     uint32_t gv[32], uv[32];
@@ -536,45 +546,38 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
                             if (col + 8 * v < p.N)
-                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
+                                *reinterpret_cast<uint4*>(orow + col + 8 * v) =
                                     make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
                     }
                 }
             } else {
+                __nv_bfloat16* split_out = reinterpret_cast<__nv_bfloat16*>(p.out[0]);
+                uint8_t* wbuf = out_stage + (warp - 2) * kOutWarpBytes;
 #pragma unroll 1
-                for (int c = half * (PBN / kSplits); c < (half + 1) * (PBN / kSplits); c += 32) {
-                    uint32_t v32[32];
-                    tmem_ld_32cols(taddr + c, v32);
-                    const int col = n * PBN + c;
-                    float cs[32];
-                    if constexpr (E4M3) load_col_scales_strided(p.col_scale0[g], p.col_scale_stride, col, p.N, cs);
-                    tmem_ld_wait();
-                    uint32_t packed[16];
+                for (int c0 = half * (PBN / kSplits); c0 < (half + 1) * (PBN / kSplits); c0 += 64) {
+                    uint32_t packed[32];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float v0 = __uint_as_float(v32[2 * j]), v1 = __uint_as_float(v32[2 * j + 1]);
-                        if constexpr (E4M3) {
-                            v0 = v0 * rs * cs[2 * j];
-                            v1 = v1 * rs * cs[2 * j + 1];
-                        }
-                        packed[j] = pack_bf16x2(v0, v1);
-                    }
-                    if (row_ok) {
-                        // the outputs are final: evict-first stores
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int c = c0 + 32 * hh;
+                        uint32_t v32[32];
+                        tmem_ld_32cols(taddr + c, v32);
+                        const int col = n * PBN + c;
+                        float cs[32];
+                        if constexpr (E4M3) load_col_scales_strided(p.col_scale0[g], p.col_scale_stride, col, p.N, cs);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int cv = col + 8 * v;
-                            if (cv >= p.N) continue;
-                            __nv_bfloat16* dst = out + cv;
-                            if (p.split_w > 0) {  // 8-column vectors never straddle blocks (split_w % 8 == 0)
-                                const int blk = cv / p.split_w;
-                                dst = reinterpret_cast<__nv_bfloat16*>(p.out[0]) + blk * p.split_stride +
-                                      static_cast<long long>(row) * p.split_w + (cv - blk * p.split_w);
+                        for (int j = 0; j < 16; ++j) {
+                            float v0 = __uint_as_float(v32[2 * j]), v1 = __uint_as_float(v32[2 * j + 1]);
+                            if constexpr (E4M3) {
+                                v0 = v0 * rs * cs[2 * j];
+                                v1 = v1 * rs * cs[2 * j + 1];
                             }
-                            __stcs(reinterpret_cast<uint4*>(dst),
-                                   make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
+                            packed[16 * hh + j] = pack_bf16x2(v0, v1);
                         }
                     }
+                    // the outputs are final: evict-first stores
+                    store_block_staged<true>(wbuf, packed, lane, out, p.ldo, split_out, p.split_w, p.split_stride,
+                                             row0, p.M, n * PBN + c0, p.N);
                 }
             }
             // The accumulator's reads are complete (tcgen05.wait::ld) and
@@ -683,7 +686,8 @@ namespace {
 template <Epi EPI, int EW, bool E4M3 = false, int ST = 6>
 cudaError_t launch_pair_typed(const TcGemmParams& p, int num_sms, cudaStream_t s) {
     auto* kfn = pair::tc_gemm_pair_kernel<EPI, EW, E4M3, ST>;
-    constexpr int PSMEM_BYTES = pair::psmem_bytes<ST>();
+    constexpr int PSMEM_BYTES = pair::psmem_bytes<EPI, ST, EW>();
+    static_assert(PSMEM_BYTES <= 227 * 1024, "pipeline and output staging do not fit in shared memory");
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, PSMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
