@@ -504,6 +504,28 @@ def timed(fn, steps, warmup, stream):
     return e0.elapsed_time(e1) / steps
 
 
+def timed_flushed(fn, steps, warmup, stream, flush):
+    """Median time of one call, each call timed alone (CUDA events on the
+    launching stream) after L2 is flushed: a buffer larger than L2 is written
+    and then read, outside the timed pair.  For workloads whose inputs fit in
+    L2, where back-to-back calls would find them there."""
+    import statistics
+    import torch
+    for _ in range(max(3, warmup)):
+        fn()
+    ev = []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
 def run_other(args):
     """Measurement lines for the Delayed-TP stack, the attention-side boundary
     and the neuron-permutation gather (one GPU, device-resident inputs)."""
@@ -531,11 +553,19 @@ def run_other(args):
             T["x_shards"].copy_(xs0)
             st.dtp_ffn_stack_forward(T["x_shards"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.L,
                                      cfg.delta, 1, cfg.eps, workspace=ws)
-        ms = timed(fn, args.steps, args.warmup, stream)
+        # the stack's weights and activations (91 MB) fit in L2: each call is
+        # timed alone after a flush; back-to-back calls are reported beside it
+        flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+        ms_warm = timed(fn, args.steps, args.warmup, stream)
+        ms = timed_flushed(fn, args.steps, args.warmup, stream, flush)
+        del flush
         fl = 6.0 * cfg.M * cfg.d * cfg.F * cfg.L
         value = fl / (ms * 1e-3) / 1e12
         line.update(metric="Delayed-TP FFN stack forward TFLOP/s", value=value, unit="TFLOP/s", ms_per_step=ms,
-                    tokens_per_s=cfg.M / (ms * 1e-3), config={"workload": cfg.name},
+                    tokens_per_s=cfg.M / (ms * 1e-3),
+                    config={"workload": cfg.name, "l2": "flushed before each call (512 MB written and read, "
+                            "not timed); value = median call"},
+                    warm_back_to_back={"ms": ms_warm, "tflops": fl / (ms_warm * 1e-3) / 1e12},
                     roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                               "frac": value / pk["bf16_sustained"], "note": "whole stack incl. the stream copy-in "
                               "(4 prologues + 8 GEMM launches + flush per step)"})
@@ -557,7 +587,9 @@ def run_other(args):
         fq, fo = 2.0 * cfg.M * cfg.d * cfg.N, 2.0 * cfg.M * cfg.Ho * cfg.d
         value = (fq + fo) / ((ms_q + ms_o) * 1e-3) / 1e12
         line.update(metric="attention-side boundary (QKV boundary + row-parallel out-projection) TFLOP/s",
-                    value=value, unit="TFLOP/s", ms_per_step=ms_q + ms_o, config={"workload": cfg.name},
+                    value=value, unit="TFLOP/s", ms_per_step=ms_q + ms_o,
+                    config={"workload": cfg.name, "l2": "inputs larger than L2 (QKV boundary 587 MB, "
+                            "out-projection 143 MB read per call)"},
                     kernels={"qkv_boundary": {"ms": ms_q, "achieved": fq / (ms_q * 1e-3) / 1e12},
                              "out_projection": {"ms": ms_o, "achieved": fo / (ms_o * 1e-3) / 1e12}},
                     roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
@@ -599,11 +631,18 @@ def run_other(args):
                 T["W1g"].data_ptr(), T["W1u"].data_ptr(), T["W2"].data_ptr(), perm.data_ptr(), cfg.L, cfg.d,
                 cfg.F, st.SPTP_BF16, outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), hdr.data_ptr(),
                 hdr.numel(), stream.cuda_stream)
-        ms = timed(fn, args.steps, args.warmup, stream)
+        # 75 MB of weights fit in L2: each call is timed alone after a flush
+        flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+        ms_warm = timed(fn, args.steps, args.warmup, stream)
+        ms = timed_flushed(fn, args.steps, args.warmup, stream, flush)
+        del flush
         by = 2.0 * 3 * cfg.L * cfg.F * cfg.d * 2
         gbs = by / (ms * 1e-3) / 1e9
         line.update(metric="neuron-permutation shard map (W1g/W1u rows + W2 columns) GB/s", value=gbs, unit="GB/s",
-                    ms_per_step=ms, config={"workload": cfg.name + "_permute"},
+                    ms_per_step=ms,
+                    config={"workload": cfg.name + "_permute", "l2": "flushed before each call (512 MB written and "
+                            "read, not timed); value = median call"},
+                    warm_back_to_back={"ms": ms_warm, "gbs": by / (ms_warm * 1e-3) / 1e9},
                     roofline={"bound": "hbm", "achieved": gbs, "peak": pk["hbm"], "unit": "GB/s",
                               "frac": gbs / pk["hbm"], "algorithmic_bytes": by})
     print(json.dumps(line), flush=True)
