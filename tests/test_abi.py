@@ -90,6 +90,7 @@ def test_dtp_rejects_bad_arguments_without_gpu(lib):
     assert call(delta=-1) == -2
     assert call(L=0) == -2
     assert call(P=8, F=8 * 64, L=40, delta=40) == -2   # too many pending sources
+    assert call(P=8, F=8 * 64, L=10, delta=9) == -2    # 1 + 7 * 10 = 71 > 64 sources in one update
     assert lib.dtp_ffn_stack_forward(None, *p[1:], 64, 128, 512, 2, 2, 1, 1, 1e-6, 0, FAKE, 1 << 40, None) == -1
 
 
