@@ -15,14 +15,17 @@
 //                 (l, m, p, n) until all gate/up tiles of (l, p, m) are stored
 //   warp 1        MMA issuer of the even CTA (M=256, N=256, K=16 UMMAs)
 //   warps 2..5    epilogue: SwiGLU into s_p or the partial o_p^(l) into the
-//                 pending ring, then a release increment of the tile's counter
+//                 pending ring (row segments staged through shared memory,
+//                 store_staged.cuh), then a release increment of the tile's
+//                 counter
 // GEMM tiles run block by block over (module, 256-row block), each block's
 // down tiles `lag` blocks after its gate/up tiles, so module l+1's first
-// blocks start while module l's last ones finish.  Every dependency points to earlier work in that order or
-// to prologue rows of the same or an earlier step, so with all CTAs resident
-// every wait ends.  A pending-ring slot is rewritten by down(l, p, m) only
-// after gate/up(l, *, m) saw every shard's step-l rows of block m normed,
-// i.e. after every reader of the slot's old contents has read them.
+// blocks start while module l's last ones finish.  Every dependency points to
+// earlier work in that order or to prologue rows of the same or an earlier
+// step, so with all CTAs resident every wait ends.  A pending-ring slot is
+// rewritten by down(l, p, m) only after gate/up(l, *, m) saw every shard's
+// step-l rows of block m normed, i.e. after every reader of the slot's old
+// contents has read them.
 //
 // Weights, y, s and the ring are addressed through 3-D / 4-D tensor maps:
 //   y    [P][M][d]      -> {d, M, P}

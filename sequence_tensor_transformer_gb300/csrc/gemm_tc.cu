@@ -20,7 +20,9 @@
 // operands (kind::f8f6f4, 128 per row) for the fp8 linear layers ("[Feature]
 // Async Tensor Parallelism for Archon Engine", "Additional Information"),
 // whose epilogue multiplies the fp32 accumulator by the token row's and the
-// output column's power-of-two scales.
+// output column's power-of-two scales.  Its plain (store) epilogue stages each
+// warp's 32 x 64 output block in shared memory and writes whole 128-byte row
+// segments (store_staged.cuh); the SwiGLU epilogue stores from registers.
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
