@@ -4,6 +4,6 @@ from .sptp_oracle import (attn_qkv_boundary, dtp_ffn_stack_forward, dtp_ffn_stac
                           permute_ffn_neurons, reduce_partials, rel_max_error, rms_norm, rowparallel_projection,
                           shard_ffn, silu, sptp_ffn_forward)
 
-__all__ = ["fp8_oracle", "attn_qkv_boundary", "dtp_ffn_stack_forward", "dtp_ffn_stack_forward_permuted", "permute_ffn_neurons",
-           "reduce_partials", "rel_max_error", "rms_norm", "rowparallel_projection", "shard_ffn", "silu",
-           "sptp_ffn_forward"]
+__all__ = ["fp8_oracle", "attn_qkv_boundary", "dtp_ffn_stack_forward", "dtp_ffn_stack_forward_permuted",
+           "permute_ffn_neurons", "reduce_partials", "rel_max_error", "rms_norm", "rowparallel_projection",
+           "shard_ffn", "silu", "sptp_ffn_forward"]

@@ -73,10 +73,6 @@ int reset_status(void* ws, cudaStream_t s) {
     return cudaMemsetAsync(ws, 0, sizeof(DeviceStatus), s) == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA;
 }
 
-
-
-
-
 // Readiness counters of the fused Delayed-TP stack: per module, rows normed
 // and down halves stored per 256-row block; gate/up halves per (shard, block).
 size_t dtp_counter_bytes(int M, int P, int L) {

@@ -533,7 +533,8 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                         for (int v = 0; v < 2; ++v)
                             if (col + 8 * v < ncols)
                                 __stcs(reinterpret_cast<uint4*>(out + col + 8 * v),
-                                       make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]));
+                                       make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                                  packed[4 * v + 3]));
                     }
                 }
             }

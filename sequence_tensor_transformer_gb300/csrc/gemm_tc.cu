@@ -305,7 +305,9 @@ static_assert(psmem_bytes<Epi::kStore, kMaxPStages, 4>() <= 227 * 1024, "pipelin
 template <bool E4M3>
 __host__ __device__ constexpr int k_elems() { return E4M3 ? 128 : 64; }
 template <bool E4M3>
-__host__ __device__ constexpr uint32_t pair_idesc() { return E4M3 ? idesc_e4m3_f32(PBM, PBN) : idesc_bf16_f32(PBM, PBN); }
+__host__ __device__ constexpr uint32_t pair_idesc() {
+    return E4M3 ? idesc_e4m3_f32(PBM, PBN) : idesc_bf16_f32(PBM, PBN);
+}
 // Epilogue warps EW: 4 (one per TMEM lane quarter) or 8 (two per quarter,
 // each taking half of the tile's columns).
 template <int EW>

@@ -139,7 +139,8 @@ cudaError_t launch_permute_ffn(const void* W1g, const void* W1u, const void* W2,
     if (grid2 > static_cast<long long>(num_sms) * 4) grid2 = static_cast<long long>(num_sms) * 4;
     auto launch = [&](auto kfn, auto tag) -> cudaError_t {
         using TT = decltype(tag);
-        cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        cudaError_t err =
+            cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (err != cudaSuccess) return err;
         kfn<<<static_cast<int>(grid2), 512, smem, s>>>(static_cast<const TT*>(W2), static_cast<TT*>(W2_out), perm, L,
                                                         d, F, st);

@@ -303,7 +303,8 @@ def test_bounded_wait_reports_timeout_without_hanging():
     check(*run_boundary(cfg), "fp32")
 
 
-@pytest.mark.parametrize("M,d,F,P,C", [(1024, 4096, 2 * 1024, 2, 2), (512, 3584, 4 * 512, 4, 4), (300, 1000, 3 * 128, 3, 3)])
+@pytest.mark.parametrize("M,d,F,P,C", [(1024, 4096, 2 * 1024, 2, 2), (512, 3584, 4 * 512, 4, 4),
+                                       (300, 1000, 3 * 128, 3, 3)])
 def test_fused_boundary_equals_three_launch_path_bitwise(M, d, F, P, C, monkeypatch):
     """With up to 5 sources and d <= 4096 the fused launch's prologue (one
     row per CTA) reduces in the standalone prologue's order and every GEMM
