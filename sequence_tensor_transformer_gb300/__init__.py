@@ -117,6 +117,31 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _expect(name, t, shape, dtype, optional=False):
+    """Shape and dtype of a tensor argument, checked before any pointer is
+    passed: the C ABI takes pointers and sizes only, so a tensor of the wrong
+    shape would otherwise be read or written past its end."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+
+
+def _same_device(*ts):
+    ts = [t for t in ts if t is not None]
+    for t in ts[1:]:
+        if t.device != ts[0].device:
+            raise ValueError(f"tensors on {ts[0].device} and {t.device}: one device expected")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -141,21 +166,37 @@ def dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dtype=SPTP_BF16) -> int:
     return int(lib().dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dtype))
 
 
+def _check_ffn_args(x, partials, gamma, W1g, W1u, W2, P, out, resid_out, dtype=None):
+    M, d = x.shape
+    F = W1g.shape[0]
+    dt = x.dtype if dtype is None else dtype
+    _expect("partials", partials, (P, M, d), dt)
+    _expect("gamma", gamma, (d,), dt)
+    _expect("W1g", W1g, (F, d), dt)
+    _expect("W1u", W1u, (F, d), dt)
+    _expect("W2", W2, (d, F), dt)
+    _expect("out", out, (P, M, d), dt, optional=True)
+    _expect("resid_out", resid_out, (M, d), dt, optional=True)
+    _same_device(x, partials, gamma, W1g, W1u, W2, out, resid_out)
+
+
 def sptp_ffn_forward(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, out=None, resid_out=None,
                      workspace=None, stream=None, write_resid=True):
     """SP-TP FFN boundary.  Returns (out [P,M,d], resid_out [M,d] or None)."""
     M, d = x.shape
     F = W1g.shape[0]
     dt = _dtype_code(x)
+    _check_ffn_args(x, partials, gamma, W1g, W1u, W2, P, out, resid_out)
     if out is None:
         out = torch.empty((P, M, d), dtype=x.dtype, device=x.device)
     if resid_out is None and write_resid:
         resid_out = torch.empty_like(x)
     if workspace is None:
         workspace = _workspace(sptp_ffn_workspace_size(M, d, F, P, chunks, dt), x.device)
+    _same_device(x, workspace)
     code = lib().sptp_ffn_forward(
         _ptr(x), _ptr(partials), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, chunks,
-        float(eps), dt, _ptr(out), _ptr(resid_out), _ptr(workspace), workspace.numel(), _stream(stream))
+        float(eps), dt, _ptr(out), _ptr(resid_out), _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check("sptp_ffn_forward", code)
     return out, resid_out
 
@@ -166,11 +207,17 @@ def dtp_ffn_stack_forward(x_shards, gamma, W1g, W1u, W2, P, L, delta, flush, eps
     _, M, d = x_shards.shape
     F = W1g.shape[1]
     dt = _dtype_code(x_shards)
+    _expect("x_shards", x_shards, (P, M, d), x_shards.dtype)
+    _expect("gamma", gamma, (L, d), x_shards.dtype)
+    _expect("W1g", W1g, (L, F, d), x_shards.dtype)
+    _expect("W1u", W1u, (L, F, d), x_shards.dtype)
+    _expect("W2", W2, (L, d, F), x_shards.dtype)
     if workspace is None:
         workspace = _workspace(dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dt), x_shards.device)
+    _same_device(x_shards, gamma, W1g, W1u, W2, workspace)
     code = lib().dtp_ffn_stack_forward(
         _ptr(x_shards), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, L, delta, int(flush),
-        float(eps), dt, _ptr(workspace), workspace.numel(), _stream(stream))
+        float(eps), dt, _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check("dtp_ffn_stack_forward", code)
     return x_shards
 
@@ -178,6 +225,11 @@ def dtp_ffn_stack_forward(x_shards, gamma, W1g, W1u, W2, P, L, delta, flush, eps
 def sptp_prologue(x, partials, gamma, eps, h_out=None, y_out=None, stream=None, write_h=True):
     M, d = x.shape
     P = partials.shape[0]
+    _expect("partials", partials, (P, M, d), x.dtype)
+    _expect("gamma", gamma, (d,), x.dtype)
+    _expect("h_out", h_out, (M, d), x.dtype, optional=True)
+    _expect("y_out", y_out, (M, d), x.dtype, optional=True)
+    _same_device(x, partials, gamma, h_out, y_out)
     if y_out is None:
         y_out = torch.empty_like(x)
     if h_out is None and write_h:
@@ -191,12 +243,16 @@ def sptp_prologue(x, partials, gamma, eps, h_out=None, y_out=None, stream=None, 
 def sptp_gateup_swiglu(y, W1g, W1u, P, s_out=None, workspace=None, stream=None):
     M, d = y.shape
     F = W1g.shape[0]
+    _expect("W1g", W1g, (F, d), y.dtype)
+    _expect("W1u", W1u, (F, d), y.dtype)
+    _expect("s_out", s_out, (P, M, F // P), y.dtype, optional=True)
     if s_out is None:
         s_out = torch.empty((P, M, F // P), dtype=y.dtype, device=y.device)
     if workspace is None:
         workspace = _workspace(SPTP_WS_HEADER_BYTES, y.device)
+    _same_device(y, W1g, W1u, s_out, workspace)
     code = lib().sptp_gateup_swiglu(_ptr(y), _ptr(W1g), _ptr(W1u), M, d, F, P, _dtype_code(y), _ptr(s_out),
-                                    _ptr(workspace), workspace.numel(), _stream(stream))
+                                    _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check("sptp_gateup_swiglu", code)
     return s_out
 
@@ -204,12 +260,16 @@ def sptp_gateup_swiglu(y, W1g, W1u, P, s_out=None, workspace=None, stream=None):
 def sptp_down_proj(s, W2, P, out=None, workspace=None, stream=None):
     _, M, f = s.shape
     d, F = W2.shape
+    _expect("s", s, (P, M, F // P), s.dtype)
+    _expect("out", out, (P, M, d), s.dtype, optional=True)
+    _expect("W2", W2, (d, F), s.dtype)
     if out is None:
         out = torch.empty((P, M, d), dtype=s.dtype, device=s.device)
     if workspace is None:
         workspace = _workspace(SPTP_WS_HEADER_BYTES, s.device)
+    _same_device(s, W2, out, workspace)
     code = lib().sptp_down_proj(_ptr(s), _ptr(W2), M, d, F, P, _dtype_code(s), _ptr(out), _ptr(workspace),
-                                workspace.numel(), _stream(stream))
+                                _nbytes(workspace), _stream(stream))
     _check("sptp_down_proj", code)
     return out
 
@@ -220,6 +280,8 @@ def sptp_ffn_forward_noalloc(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, o
     device allocation inside the call; the caller passes out/resid_out)."""
     M, d = x.shape
     F = W1g.shape[0]
+    _check_ffn_args(x, partials, gamma, W1g, W1u, W2, P, out, resid_out)
+    _expect("out", out, (P, M, d), x.dtype)
     code = lib().sptp_ffn_forward_noalloc(
         _ptr(x), _ptr(partials), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, chunks, float(eps),
         _dtype_code(x), _ptr(out), _ptr(resid_out), _stream(stream))
@@ -237,6 +299,12 @@ def sptp_attn_qkv_forward(x, partials, gamma, Wqkv, P, chunks, eps, qkv_out=None
     M, d = x.shape
     N = Wqkv.shape[0]
     dt = _dtype_code(x)
+    _expect("partials", partials, (P, M, d), x.dtype)
+    _expect("gamma", gamma, (d,), x.dtype)
+    _expect("Wqkv", Wqkv, (N, d), x.dtype)
+    _expect("qkv_out", qkv_out, (P, M, N // P), x.dtype, optional=True)
+    _expect("resid_out", resid_out, (M, d), x.dtype, optional=True)
+    _same_device(x, partials, gamma, Wqkv, qkv_out, resid_out, workspace)
     if qkv_out is None:
         qkv_out = torch.empty((P, M, N // P), dtype=x.dtype, device=x.device)
     if resid_out is None and write_resid:
@@ -245,7 +313,7 @@ def sptp_attn_qkv_forward(x, partials, gamma, Wqkv, P, chunks, eps, qkv_out=None
         workspace = _workspace(sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dt), x.device)
     code = lib().sptp_attn_qkv_forward(_ptr(x), _ptr(partials), _ptr(gamma), _ptr(Wqkv), M, d, N, P, chunks,
                                        float(eps), dt, _ptr(qkv_out), _ptr(resid_out), _ptr(workspace),
-                                       workspace.numel(), _stream(stream))
+                                       _nbytes(workspace), _stream(stream))
     _check("sptp_attn_qkv_forward", code)
     return qkv_out, resid_out
 
@@ -254,14 +322,16 @@ def sptp_permute_ffn_neurons(W1g, W1u, W2, perm, workspace=None, stream=None):
     """Renumbers every module's neurons (W1g/W1u [L,F,d] rows, W2 [L,d,F]
     columns) by perm [L,F] (int32, device); returns the permuted copies."""
     L, F, d = W1g.shape
-    outs = [torch.empty_like(W1g), torch.empty_like(W1u), torch.empty_like(W2)]
+    _expect("W1u", W1u, (L, F, d), W1g.dtype)
+    _expect("W2", W2, (L, d, F), W1g.dtype)
+    _expect("perm", perm, (L, F), torch.int32)
     if workspace is None:
         workspace = _workspace(SPTP_WS_HEADER_BYTES, W1g.device)
-    if perm.dtype != torch.int32:
-        raise TypeError("perm must be int32")
+    _same_device(W1g, W1u, W2, perm, workspace)
+    outs = [torch.empty_like(W1g), torch.empty_like(W1u), torch.empty_like(W2)]
     code = lib().sptp_permute_ffn_neurons(_ptr(W1g), _ptr(W1u), _ptr(W2), _ptr(perm), L, d, F, _dtype_code(W1g),
                                           _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _ptr(workspace),
-                                          workspace.numel(), _stream(stream))
+                                          _nbytes(workspace), _stream(stream))
     _check("sptp_permute_ffn_neurons", code)
     return tuple(outs)
 
@@ -271,7 +341,7 @@ def sptp_read_device_status(workspace, stream=None) -> int:
 
 
 def sptp_wait_selftest(workspace, limit_ns: int, preset_flag: bool, stream=None) -> int:
-    return int(lib().sptp_wait_selftest(_ptr(workspace), workspace.numel(), int(limit_ns), int(preset_flag),
+    return int(lib().sptp_wait_selftest(_ptr(workspace), _nbytes(workspace), int(limit_ns), int(preset_flag),
                                         _stream(stream)))
 
 
@@ -285,6 +355,9 @@ def sptp_quantize_rows_e4m3(a, q=None, scale=None, stream=None):
         raise TypeError("bf16 input expected")
     K = a.shape[-1]
     R = a.numel() // K if K else 0
+    _expect("q", q, tuple(a.shape), torch.uint8, optional=True)
+    _expect("scale", scale, tuple(a.shape[:-1]), torch.float32, optional=True)
+    _same_device(a, q, scale)
     if q is None:
         q = torch.empty(a.shape, dtype=torch.uint8, device=a.device)
     if scale is None:
@@ -299,6 +372,10 @@ def quantize_ffn_weights_e4m3(W1g, W1u, W2, P, stream=None):
     (qW1g, sW1g [F], qW1u, sW1u [F], qW2 [d,F], sW2 [d,P]); W2 is quantised as
     [d*P][F/P] rows, one scale per output feature and shard."""
     d, F = W2.shape
+    _expect("W1g", W1g, (F, d), torch.bfloat16)
+    _expect("W1u", W1u, (F, d), torch.bfloat16)
+    if F % P != 0:
+        raise ValueError(f"F = {F} is not a multiple of P = {P}")
     qg, sg = sptp_quantize_rows_e4m3(W1g, stream=stream)
     qu, su = sptp_quantize_rows_e4m3(W1u, stream=stream)
     q2, s2 = sptp_quantize_rows_e4m3(W2.view(d, P, F // P), stream=stream)
@@ -316,6 +393,17 @@ def sptp_ffn_forward_fp8(x, partials, gamma, qweights, P, chunks, eps, out=None,
     qg, sg, qu, su, q2, s2 = qweights
     M, d = x.shape
     F = qg.shape[0]
+    bf = torch.bfloat16
+    _expect("x", x, (M, d), bf)
+    _expect("partials", partials, (P, M, d), bf)
+    _expect("gamma", gamma, (d,), bf)
+    for name, t, shape, dt in (("qW1g", qg, (F, d), torch.uint8), ("sW1g", sg, (F,), torch.float32),
+                               ("qW1u", qu, (F, d), torch.uint8), ("sW1u", su, (F,), torch.float32),
+                               ("qW2", q2, (d, F), torch.uint8), ("sW2", s2, (d, P), torch.float32)):
+        _expect(name, t, shape, dt)
+    _expect("out", out, (P, M, d), bf, optional=True)
+    _expect("resid_out", resid_out, (M, d), bf, optional=True)
+    _same_device(x, partials, gamma, qg, sg, qu, su, q2, s2, out, resid_out, workspace)
     if out is None:
         out = torch.empty((P, M, d), dtype=x.dtype, device=x.device)
     if resid_out is None and write_resid:
@@ -324,7 +412,7 @@ def sptp_ffn_forward_fp8(x, partials, gamma, qweights, P, chunks, eps, out=None,
         workspace = _workspace(sptp_ffn_fp8_workspace_size(M, d, F, P, chunks), x.device)
     code = lib().sptp_ffn_forward_fp8(
         _ptr(x), _ptr(partials), _ptr(gamma), _ptr(qg), _ptr(sg), _ptr(qu), _ptr(su), _ptr(q2), _ptr(s2), M, d, F,
-        P, chunks, float(eps), _ptr(out), _ptr(resid_out), _ptr(workspace), workspace.numel(), _stream(stream))
+        P, chunks, float(eps), _ptr(out), _ptr(resid_out), _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check("sptp_ffn_forward_fp8", code)
     return out, resid_out
 
@@ -335,6 +423,15 @@ def sptp_prologue_e4m3(x, partials, gamma, eps, h_out=None, y_work=None, q_out=N
     launch.  Returns (h or None, q uint8 [M,d], scale float32 [M])."""
     M, d = x.shape
     P = partials.shape[0]
+    bf = torch.bfloat16
+    _expect("x", x, (M, d), bf)
+    _expect("partials", partials, (P, M, d), bf)
+    _expect("gamma", gamma, (d,), bf)
+    _expect("h_out", h_out, (M, d), bf, optional=True)
+    _expect("y_work", y_work, (M, d), bf, optional=True)
+    _expect("q_out", q_out, (M, d), torch.uint8, optional=True)
+    _expect("scale_out", scale_out, (M,), torch.float32, optional=True)
+    _same_device(x, partials, gamma, h_out, y_work, q_out, scale_out)
     if h_out is None and write_h:
         h_out = torch.empty_like(x)
     if y_work is None:
@@ -352,12 +449,18 @@ def sptp_prologue_e4m3(x, partials, gamma, eps, h_out=None, y_work=None, q_out=N
 def sptp_gateup_swiglu_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, P, s_out=None, workspace=None, stream=None):
     M, d = qy.shape
     F = qW1g.shape[0]
+    for name, t, shape, dt in (("qy", qy, (M, d), torch.uint8), ("sy", sy, (M,), torch.float32),
+                               ("qW1g", qW1g, (F, d), torch.uint8), ("sW1g", sW1g, (F,), torch.float32),
+                               ("qW1u", qW1u, (F, d), torch.uint8), ("sW1u", sW1u, (F,), torch.float32)):
+        _expect(name, t, shape, dt)
+    _expect("s_out", s_out, (P, M, F // P), torch.bfloat16, optional=True)
+    _same_device(qy, sy, qW1g, sW1g, qW1u, sW1u, s_out, workspace)
     if s_out is None:
         s_out = torch.empty((P, M, F // P), dtype=torch.bfloat16, device=qy.device)
     if workspace is None:
         workspace = _workspace(SPTP_WS_HEADER_BYTES, qy.device)
     code = lib().sptp_gateup_swiglu_e4m3(_ptr(qy), _ptr(sy), _ptr(qW1g), _ptr(sW1g), _ptr(qW1u), _ptr(sW1u), M, d,
-                                         F, P, _ptr(s_out), _ptr(workspace), workspace.numel(), _stream(stream))
+                                         F, P, _ptr(s_out), _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check("sptp_gateup_swiglu_e4m3", code)
     return s_out
 
@@ -365,11 +468,16 @@ def sptp_gateup_swiglu_e4m3(qy, sy, qW1g, sW1g, qW1u, sW1u, P, s_out=None, works
 def sptp_down_proj_e4m3(qs, ss, qW2, sW2, P, out=None, workspace=None, stream=None):
     _, M, f = qs.shape
     d, F = qW2.shape
+    for name, t, shape, dt in (("qs", qs, (P, M, F // P), torch.uint8), ("ss", ss, (P, M), torch.float32),
+                               ("qW2", qW2, (d, F), torch.uint8), ("sW2", sW2, (d, P), torch.float32)):
+        _expect(name, t, shape, dt)
+    _expect("out", out, (P, M, d), torch.bfloat16, optional=True)
+    _same_device(qs, ss, qW2, sW2, out, workspace)
     if out is None:
         out = torch.empty((P, M, d), dtype=torch.bfloat16, device=qs.device)
     if workspace is None:
         workspace = _workspace(SPTP_WS_HEADER_BYTES, qs.device)
     code = lib().sptp_down_proj_e4m3(_ptr(qs), _ptr(ss), _ptr(qW2), _ptr(sW2), M, d, F, P, _ptr(out),
-                                     _ptr(workspace), workspace.numel(), _stream(stream))
+                                     _ptr(workspace), _nbytes(workspace), _stream(stream))
     _check("sptp_down_proj_e4m3", code)
     return out
