@@ -38,6 +38,28 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(st.EXPORTED_SYMBOLS)
 
 
+def test_every_declared_function_is_documented():
+    """Each entry point of include/sptp.h sits under a comment block (argument
+    meaning, layout, ownership, errors): one directly above it, or the one
+    above the group of declarations it belongs to."""
+    src = open(os.path.join(ROOT, "include", "sptp.h")).read()
+    decls = [(m.start(), m.group(1)) for m in re.finditer(
+        r"^(?:const\s+)?(?:size_t|int|void|const char\s*\*)\s*\*?\s*(\w+)\s*\(", src, re.M)]
+    assert len(decls) >= 20
+    documented = set()
+    for pos, name in decls:
+        before = src[:pos].rstrip()
+        if before.endswith("*/"):
+            documented.add(pos)
+        elif before.endswith(");"):
+            # part of a group: the declaration just above must be documented
+            prev = max(p for p, _ in decls if p < pos)
+            assert prev in documented, name
+            documented.add(pos)
+        else:
+            raise AssertionError(f"{name} has no comment block")
+
+
 def test_status_strings(lib):
     assert st.sptp_status_string(0) == "ok"
     for c in range(-1, -9, -1):
