@@ -237,11 +237,28 @@ def dtp_ffn_stack_forward_permuted(x_shards, gamma, W1g, W1u, W2, perms, P: int,
 
 
 def rel_max_error(got: np.ndarray, ref: np.ndarray) -> float:
-    """max_i |got_i - ref_i| / max_i |ref_i| (0 when both are all zero)."""
+    """The parity metric: max_i |got_i - ref_i| / max_i |ref_i| over one output
+    tensor, element i of `got` against element i of `ref` (the workloads'
+    "rel. max error"; absolute max error when `ref` is all zero, 0 when both
+    are).
+
+    The two arrays must have the same shape (no broadcasting: a single row
+    compared with a whole tensor is an error, not a pass).  A non-finite
+    element of `got` gives +inf, so it fails every bound and sorts above
+    every finite error; a non-finite `ref` is a fault of the reference and
+    raises."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    den = float(np.max(np.abs(ref))) if ref.size else 0.0
-    num = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    if got.shape != ref.shape:
+        raise ValueError(f"shapes differ: got {got.shape}, ref {ref.shape}")
+    if not np.all(np.isfinite(ref)):
+        raise ValueError("the reference holds non-finite values")
+    if ref.size == 0:
+        return 0.0
+    if not np.all(np.isfinite(got)):
+        return float("inf")
+    num = float(np.max(np.abs(got - ref)))
+    den = float(np.max(np.abs(ref)))
     if den == 0.0:
         return num
     return num / den

@@ -425,3 +425,74 @@ def test_attn_qkv_boundary_chunking_and_zero_weights():
     assert rel_max_error(a, b) < 1e-14 and rel_max_error(ha, hb) == 0.0
     z, _ = oracle.attn_qkv_boundary(x, parts, gamma, np.zeros_like(W), P, P, 1e-6)
     assert np.all(z == 0)
+
+
+# ---------------------------------------------------------------- the parity metric
+# rel_max_error is the comparison behind every parity assertion, so it is
+# pinned to hand-computed values: max_i |got_i - ref_i| / max_i |ref_i|.
+
+def test_rel_max_error_closed_form():
+    assert rel_max_error(np.array([1.0, 2.0]), np.array([1.0, 4.0])) == 0.5
+    # a 2-D tensor: the max runs over every element
+    assert rel_max_error(np.array([[1.0, 2.0], [3.0, 4.5]]), np.array([[1.0, 2.0], [3.0, 5.0]])) == 0.1
+
+
+def test_rel_max_error_takes_the_absolute_difference():
+    # the largest error is negative (got below ref); a signed max would say 0
+    assert rel_max_error(np.array([0.0, 10.0]), np.array([3.0, 10.0])) == 0.3
+    # and positive (got above ref); a max of (ref - got) would say 0
+    assert rel_max_error(np.array([5.0, 10.0]), np.array([3.0, 10.0])) == 0.2
+    # a negative error larger in magnitude than a positive one
+    assert rel_max_error(np.array([1.5, 6.0]), np.array([1.0, 10.0])) == 0.4
+
+
+def test_rel_max_error_normalises_by_the_reference():
+    # by max|ref| = 2, not by max|got| = 1
+    assert rel_max_error(np.array([0.0, 1.0]), np.array([0.0, 2.0])) == 0.5
+    # by max|ref| = 4, not by max(ref) = 1 (the largest reference is negative)
+    assert rel_max_error(np.array([-4.0, 2.0]), np.array([-4.0, 1.0])) == 0.25
+    # symmetric in sign: negating both changes nothing
+    assert rel_max_error(-np.array([-4.0, 2.0]), -np.array([-4.0, 1.0])) == 0.25
+
+
+def test_rel_max_error_is_a_max_not_a_mean():
+    ref = np.ones(1001)
+    got = ref.copy()
+    got[517] += 0.5
+    assert rel_max_error(got, ref) == 0.5
+
+
+def test_rel_max_error_pairs_elements_by_index():
+    # the same multiset of values in another order is an error of 2 / 3
+    assert rel_max_error(np.array([1.0, 2.0, 3.0]), np.array([3.0, 2.0, 1.0])) == pytest.approx(2.0 / 3.0, abs=0)
+
+
+def test_rel_max_error_zero_cases():
+    assert rel_max_error(np.zeros(5), np.zeros(5)) == 0.0
+    # an all-zero reference: the absolute error
+    assert rel_max_error(np.array([0.0, -0.25, 0.0]), np.zeros(3)) == 0.25
+    assert rel_max_error(np.zeros((0, 4)), np.zeros((0, 4))) == 0.0
+    assert rel_max_error(np.array([2.0, 3.0]), np.array([2.0, 3.0])) == 0.0
+
+
+def test_rel_max_error_fails_non_finite_outputs():
+    ref = np.array([1.0, 2.0, 3.0])
+    for bad in (np.nan, np.inf, -np.inf):
+        got = ref.copy()
+        got[1] = bad
+        err = rel_max_error(got, ref)
+        assert err == math.inf and not err <= 2e-2
+    # inf sorts above every finite error, wherever it sits in a list
+    assert max([rel_max_error(np.array([np.nan]), np.array([1.0])), 0.5]) == math.inf
+    with pytest.raises(ValueError):
+        rel_max_error(ref, np.array([1.0, np.nan, 3.0]))
+
+
+def test_rel_max_error_rejects_shape_mismatch():
+    ref = np.arange(12.0).reshape(4, 3)
+    with pytest.raises(ValueError):
+        rel_max_error(ref[:1], ref)          # one row against a whole tensor
+    with pytest.raises(ValueError):
+        rel_max_error(ref, ref.T)
+    with pytest.raises(ValueError):
+        rel_max_error(ref.reshape(-1), ref)
