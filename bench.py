@@ -39,6 +39,12 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", choices=["auto", "pair", "chain", "fused"], default="auto",
+                    help="launch variant of the boundary call (sptp_variant); auto is the library's default")
+    ap.add_argument("--sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back boundary calls for the power-capped (sustained) figure")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' figures (the 'configs' key)")
     ap.add_argument("--workload", choices=["boundary", "dtp", "attn", "permute", "fp8", "msweep", "qwen2"],
                     default="boundary",
                     help="boundary: the SP-TP FFN boundary (the default, headline line); the others measure "
@@ -82,15 +88,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 200):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -286,12 +293,8 @@ def run_ours(args):
     st.load_library()
     cfg = workload()
     M, d, F, P, C = cfg.M, cfg.d, cfg.F, cfg.P, cfg.chunks
-    inp = synth.boundary_inputs(cfg)
-
-    def to_dev(a):
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    T = {k: to_dev(v) for k, v in inp.items()}
+    variant = args.variant
+    T = boundary_tensors(cfg, dev)
     out = torch.empty((P, M, d), dtype=torch.bfloat16, device=dev)
     resid = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(st.sptp_ffn_workspace_size(M, d, F, P, C, st.SPTP_BF16), dtype=torch.uint8, device=dev)
@@ -299,13 +302,13 @@ def run_ours(args):
 
     def step():
         st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P, C, cfg.eps,
-                            out=out, resid_out=resid, workspace=ws)
+                            out=out, resid_out=resid, workspace=ws, variant=variant)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     if st.sptp_read_device_status(ws) != 0:
-        raise RuntimeError("device status reports a timeout")
+        raise RuntimeError("device status reports a failed wait")
 
     # ---------------- timed region: K whole-boundary steps
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -319,51 +322,28 @@ def run_ours(args):
         torch.cuda.synchronize()
     barrier(pg, dev)
     ms_total = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+    if st.sptp_read_device_status(ws) != 0:
+        raise RuntimeError("device status reports a failed wait")
     out_ref, resid_ref = out.clone(), resid.clone()  # the timed call's results
     ms_step = ms_total / args.steps
     fl = flops_per_step(cfg)
     value = fl * world / (ms_step * 1e-3) / 1e12
     tokens = M * world / (ms_step * 1e-3)
+    pk = peaks()
+    # The denominator fits the regime the number was taken in: a region of
+    # under a second runs at full clock (the burst peak); seconds of
+    # back-to-back calls run under the power cap (the sustained peak, the
+    # "sustained" key below).
+    peak_k, kind_k = peak_for(pk, ms_total)
 
-    # ---------------- per-kernel durations: the same three kernels launched
-    # through the step-level entry points with events between them
-    y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
-    s_buf = torch.empty((P, M, F // P), dtype=torch.bfloat16, device=dev)
-    hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
-    n_k = min(args.steps, 200)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_k)]
-    for _ in range(3):
-        st.sptp_prologue(T["x"], T["partials"], T["gamma"], cfg.eps, h_out=resid, y_out=y)
-        st.sptp_gateup_swiglu(y, T["W1g"], T["W1u"], P, s_out=s_buf, workspace=hdr)
-        st.sptp_down_proj(s_buf, T["W2"], P, out=out, workspace=hdr)
-    torch.cuda.synchronize()
-    for i in range(n_k):
-        ev[i][0].record(stream)
-        st.sptp_prologue(T["x"], T["partials"], T["gamma"], cfg.eps, h_out=resid, y_out=y)
-        ev[i][1].record(stream)
-        st.sptp_gateup_swiglu(y, T["W1g"], T["W1u"], P, s_out=s_buf, workspace=hdr)
-        ev[i][2].record(stream)
-        st.sptp_down_proj(s_buf, T["W2"], P, out=out, workspace=hdr)
-        ev[i][3].record(stream)
-    torch.cuda.synchronize()
-    ms = {k: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(n_k))
-          for j, k in enumerate(("prologue", "gateup_swiglu", "down_proj"))}
-    # the prologue alone: reading a 512 MB buffer before each launch leaves
-    # L2 holding clean lines only -- neither the prologue's inputs nor dirty
-    # lines of another kernel that it would have to write back
+    # ---------------- the dominant kernel, timed live: the step's launches,
+    # each bracketed by CUDA events on the launching stream
+    kernels, roofline = kernel_timings(args, st, T, cfg, variant, out, resid, ws, stream, dev, pk)
+
+    # ---------------- single calls, each timed alone: with L2 as the
+    # previous call left it, and after reading 512 MB (L2 clean; the flush
+    # itself is not timed)
     flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
-    iso = []
-    for i in range(max(3, n_k // 4) + 3):
-        flush.sum()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        st.sptp_prologue(T["x"], T["partials"], T["gamma"], cfg.eps, h_out=resid, y_out=y)
-        b.record(stream)
-        iso.append((a, b))
-    torch.cuda.synchronize()
-    ms_pro_iso = statistics.median(a.elapsed_time(b) for a, b in iso[3:])
-    # single calls, each timed alone: with L2 as the previous call left it, and
-    # after reading 512 MB (L2 clean; the flush itself is not timed)
     calls = {"warm": [], "l2_flushed": []}
     for kind, lst in calls.items():
         for i in range(23):
@@ -379,35 +359,12 @@ def run_ours(args):
     for kind, lst in calls.items():
         t = [a.elapsed_time(b) for a, b in lst[3:]]
         per_call[kind] = {"calls": len(t), "median_ms": statistics.median(t), "min_ms": min(t),
-                          "median_tflops": flops_per_step(cfg) / (statistics.median(t) * 1e-3) / 1e12}
+                          "median_tflops": fl / (statistics.median(t) * 1e-3) / 1e12}
     del flush
-    pk = peaks()
-    gate_fl = 4.0 * M * d * F
-    down_fl = 2.0 * M * F * d
-    pro_bytes = ((P + 1) * M * d + 2 * M * d) * 2 + 2 * d
-    kernels = {
-        "prologue": {"ms": ms["prologue"], "bound": "hbm", "algorithmic_bytes": pro_bytes,
-                     "achieved": pro_bytes / (ms["prologue"] * 1e-3) / 1e9, "unit": "GB/s",
-                     "peak": pk["hbm"], "traffic": kernel_traffic("prologue"),
-                     "note": "inside the step it also writes back the previous down GEMM's dirty L2 lines"},
-        "prologue_isolated": {"ms": ms_pro_iso, "bound": "hbm", "algorithmic_bytes": pro_bytes,
-                              "achieved": pro_bytes / (ms_pro_iso * 1e-3) / 1e9, "unit": "GB/s",
-                              "peak": pk["hbm"], "note": "median of launches, each after reading 512 MB (L2 clean)"},
-        "gateup_swiglu": {"ms": ms["gateup_swiglu"], "bound": "tensor", "algorithmic_flops": gate_fl,
-                          "achieved": gate_fl / (ms["gateup_swiglu"] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                          "peak": pk["bf16_sustained"], "traffic": kernel_traffic("gateup_swiglu")},
-        "down_proj": {"ms": ms["down_proj"], "bound": "tensor", "algorithmic_flops": down_fl,
-                      "achieved": down_fl / (ms["down_proj"] * 1e-3) / 1e12, "unit": "TFLOP/s",
-                      "peak": pk["bf16_sustained"], "traffic": kernel_traffic("down_proj")},
-    }
-    for k in kernels.values():
-        k["frac"] = k["achieved"] / k["peak"]
-    top = kernels["gateup_swiglu"]
-    roofline = {"bound": "tensor", "kernel": "tc_gemm_pair_kernel<SwiGLU> (gate/up + SwiGLU)",
-                "achieved": top["achieved"], "peak": top["peak"], "unit": "TFLOP/s", "frac": top["frac"],
-                "traffic": top["traffic"],
-                "peak_kind": f"bf16_tflops_sustained ({pk['source']}); burst frac "
-                             f"{top['achieved'] / pk['bf16_burst']:.3f}"}
+
+    # ---------------- sustained: seconds of back-to-back calls under the
+    # power cap, with the SM clock sampled every 100 ms
+    sustained = sustained_leg(args, step, stream, dev, pg, pk, fl, world)
 
     # ---------------- end to end through the public call with host buffers:
     # every step copies its activations in from pinned host memory and its
@@ -443,7 +400,7 @@ def run_ours(args):
             stream.wait_event(ev_in[k])
             stream.wait_event(ev_out[k])             # step i-2's results are out
             st.sptp_ffn_forward(b["x"], b["p"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P, C, cfg.eps,
-                                out=b["out"], resid_out=b["h"], workspace=b["ws"])
+                                out=b["out"], resid_out=b["h"], workspace=b["ws"], variant=variant)
             ev_done[k].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[k])
@@ -463,31 +420,396 @@ def run_ours(args):
     ms_e2e = max_over_ranks(pg, t_start.elapsed_time(t_end), dev) / n_e
     # the pipeline's results match the device-resident run of the same call
     assert torch.equal(out_h, out_ref.cpu()) and torch.equal(res_h, resid_ref.cpu())
-    del out_ref, resid_ref
+    del out_ref, resid_ref, bufs
     h2d = (pin_x.numel() + pin_p.numel()) * 2
     d2h = (out_h.numel() + res_h.numel()) * 2
     e2e = {"value": fl * world / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
            "tokens_per_s": M * world / (ms_e2e * 1e-3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": n_e, "pipeline": "copies in/out on separate streams overlap the neighbouring steps' compute"}
+    del T, out, resid, ws
+    torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)
+
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = configs_leg(args, st, synth, dev, stream, pk)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1)-family init)",
                 "tokens_per_s": tokens,
-                "frac_of_bf16_peak": {"sustained": value / world / pk["bf16_sustained"],
-                                      "burst": value / world / pk["bf16_burst"]},
-                "config": config_json(cfg, {"parallelism": f"replicas x{world} (P={P} shards emulated per GPU)"}),
-                "roofline": roofline, "kernels": kernels, "per_call": per_call, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 3 * args.steps, "clocks": clk.summary()}
+                "frac_of_bf16_peak": {"value": value / world / peak_k, "peak_kind": kind_k,
+                                      "burst": value / world / pk["bf16_burst"],
+                                      "sustained": value / world / pk["bf16_sustained"]},
+                "config": config_json(cfg, {"parallelism": f"replicas x{world} (P={P} shards emulated per GPU)",
+                                            "variant": variant}),
+                "roofline": roofline, "kernels": kernels, "per_call": per_call, "sustained": sustained,
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": LAUNCHES_PER_STEP[variant] * args.steps,
+                "clocks": clk.summary(), "configs": configs}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
     return 0
+
+
+# kernels of this library launched by one boundary call, per variant (the
+# status and counter resets are memsets, not kernels)
+LAUNCHES_PER_STEP = {"auto": 3, "pair": 3, "chain": 2, "fused": 1}
+
+
+def peak_for(pk, region_ms):
+    """The bf16 denominator for a measurement over region_ms of back-to-back
+    work: under a second the GPU holds its full clock (burst), longer the
+    power cap sets it (sustained)."""
+    if region_ms < 1000.0:
+        return pk["bf16_burst"], f"bf16_tflops burst ({pk['source']}): a {region_ms:.0f} ms region"
+    return pk["bf16_sustained"], f"bf16_tflops_sustained ({pk['source']}): a {region_ms:.0f} ms region"
+
+
+def boundary_tensors(cfg, dev):
+    import torch
+    from sequence_tensor_transformer_gb300 import synth
+    inp = synth.boundary_inputs(cfg)
+    return {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in inp.items()}
+
+
+def kernel_timings(args, st, T, cfg, variant, out, resid, ws, stream, dev, pk):
+    """Per-kernel durations of one step and the roofline of the dominant one.
+    PAIR (and AUTO): the prologue, gate/up and down launches through the
+    step-level entry points, with events between them.  FUSED / CHAIN: the
+    persistent launch is the step (CHAIN: after the prologue launch)."""
+    import torch
+    M, d, F, P = cfg.M, cfg.d, cfg.F, cfg.P
+    n_k = max(3, min(args.steps, 200))
+    gate_fl, down_fl = 4.0 * M * d * F, 2.0 * M * F * d
+    pro_bytes = ((P + 1) * M * d + 2 * M * d) * 2 + 2 * d
+    y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    s_buf = torch.empty((P, M, F // P), dtype=torch.bfloat16, device=dev)
+    hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
+
+    def prologue():
+        st.sptp_prologue(T["x"], T["partials"], T["gamma"], cfg.eps, h_out=resid, y_out=y)
+
+    def gateup():
+        st.sptp_gateup_swiglu(y, T["W1g"], T["W1u"], P, s_out=s_buf, workspace=hdr)
+
+    def down():
+        st.sptp_down_proj(s_buf, T["W2"], P, out=out, workspace=hdr)
+
+    parts = [("prologue", prologue), ("gateup_swiglu", gateup), ("down_proj", down)]
+    for _ in range(3):
+        for _, fn in parts:
+            fn()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(n_k)]
+    for i in range(n_k):
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(parts):
+            fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = {k: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(n_k))
+          for j, (k, _) in enumerate(parts)}
+    region_ms = ev[0][0].elapsed_time(ev[-1][-1])
+    peak, kind = peak_for(pk, region_ms)
+    # the prologue alone: reading a 512 MB buffer before each launch leaves
+    # L2 holding clean lines only -- neither the prologue's inputs nor dirty
+    # lines of another kernel that it would have to write back
+    flush = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+    iso = []
+    for i in range(max(3, n_k // 4) + 3):
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        prologue()
+        b.record(stream)
+        iso.append((a, b))
+    torch.cuda.synchronize()
+    del flush
+    ms_pro_iso = statistics.median(a.elapsed_time(b) for a, b in iso[3:])
+    kernels = {
+        "prologue": {"ms": ms["prologue"], "bound": "hbm", "algorithmic_bytes": pro_bytes,
+                     "achieved": pro_bytes / (ms["prologue"] * 1e-3) / 1e9, "unit": "GB/s",
+                     "peak": pk["hbm"], "traffic": kernel_traffic("prologue"),
+                     "note": "inside the step it also writes back the previous down GEMM's dirty L2 lines"},
+        "prologue_isolated": {"ms": ms_pro_iso, "bound": "hbm", "algorithmic_bytes": pro_bytes,
+                              "achieved": pro_bytes / (ms_pro_iso * 1e-3) / 1e9, "unit": "GB/s",
+                              "peak": pk["hbm"], "note": "median of launches, each after reading 512 MB (L2 clean)"},
+        "gateup_swiglu": {"ms": ms["gateup_swiglu"], "bound": "tensor", "algorithmic_flops": gate_fl,
+                          "achieved": gate_fl / (ms["gateup_swiglu"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                          "peak": peak, "traffic": kernel_traffic("gateup_swiglu")},
+        "down_proj": {"ms": ms["down_proj"], "bound": "tensor", "algorithmic_flops": down_fl,
+                      "achieved": down_fl / (ms["down_proj"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "peak": peak, "traffic": kernel_traffic("down_proj")},
+    }
+    for k in kernels.values():
+        k["frac"] = k["achieved"] / k["peak"]
+    top = kernels["gateup_swiglu"]
+    roofline = {"bound": "tensor", "kernel": "tc_gemm_pair_kernel<SwiGLU> (gate/up + SwiGLU)",
+                "achieved": top["achieved"], "peak": top["peak"], "unit": "TFLOP/s", "frac": top["frac"],
+                "traffic": top["traffic"], "peak_kind": kind,
+                "frac_of_sustained": top["achieved"] / pk["bf16_sustained"]}
+    if variant in ("fused", "chain"):
+        # the persistent launch is the dominant kernel of these variants: time
+        # it as the step (CHAIN: minus its prologue launch, measured above)
+        key = "boundary_fused_kernel"
+        evs = []
+        for _ in range(n_k):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if variant == "chain":
+                prologue()
+            a.record(stream)
+            if variant == "chain":
+                st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P,
+                                    cfg.chunks, cfg.eps, out=out, resid_out=resid, workspace=ws, variant="chain")
+            else:
+                st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P,
+                                    cfg.chunks, cfg.eps, out=out, resid_out=resid, workspace=ws, variant="fused")
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        t = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        if variant == "chain":
+            t -= ms["prologue"]
+        fl = 6.0 * M * d * F
+        kernels[key] = {"ms": t, "bound": "tensor", "algorithmic_flops": fl,
+                        "achieved": fl / (t * 1e-3) / 1e12, "unit": "TFLOP/s", "peak": peak,
+                        "frac": fl / (t * 1e-3) / 1e12 / peak}
+        roofline = {"bound": "tensor", "kernel": key + (" (gate/up + down tiles)" if variant == "chain" else
+                                                        " (prologue warps + gate/up + down tiles)"),
+                    "achieved": kernels[key]["achieved"], "peak": peak, "unit": "TFLOP/s",
+                    "frac": kernels[key]["frac"], "traffic": None, "peak_kind": kind,
+                    "frac_of_sustained": kernels[key]["achieved"] / pk["bf16_sustained"]}
+    return kernels, roofline
+
+
+def sustained_leg(args, step, stream, dev, pg, pk, fl, world):
+    """Seconds of back-to-back boundary calls: the power-capped regime.  The
+    clock is sampled every 100 ms during the region."""
+    import torch
+    if args.sustained_s <= 0:
+        return None
+    # calls for about sustained_s seconds, from a short probe
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    n = max(10, int(args.sustained_s * 1e3 / (a.elapsed_time(b) / 5)))
+    barrier(pg, dev)
+    with ClockSampler(dev.index, period_ms=100) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(pg, e0.elapsed_time(e1), dev) / n
+    value = fl * world / (ms * 1e-3) / 1e12
+    c = clk.summary() or {}
+    mhz = c.get("sm_mhz")
+    return {"seconds": ms * n / 1e3, "calls": n, "ms_per_step": ms, "value": value, "unit": UNIT,
+            "frac": value / world / pk["bf16_sustained"],
+            "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
+            "clocks": c, "sm_mhz_median": mhz,
+            "ms_x_mhz": ms * mhz if mhz else None,
+            "note": "ms_x_mhz = milliseconds per step x median SM MHz = thousands of SM cycles per step"}
+
+
+# ------------------------------------------------------------------ the other workloads
+
+def time_calls(fn, stream, seconds=0.3, min_calls=5, warmup=3):
+    """Mean ms of back-to-back calls over about `seconds` (CUDA events on the
+    launching stream)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    n = max(min_calls, int(seconds * 1e3 / max(a.elapsed_time(b), 1e-3)))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n, n
+
+
+def leg_boundary(st, cfg, T, dev, stream, pk, variant="auto", seconds=0.3, parity=None):
+    """sptp_ffn_forward on one boundary workload (device-resident inputs)."""
+    import torch
+    out = torch.empty((cfg.P, cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
+    h = torch.empty_like(T["x"])
+    ws = torch.empty(st.sptp_ffn_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.chunks, st.SPTP_BF16),
+                     dtype=torch.uint8, device=dev)
+
+    def fn():
+        st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.chunks,
+                            cfg.eps, out=out, resid_out=h, workspace=ws, variant=variant)
+    ms, n = time_calls(fn, stream, seconds)
+    status = st.sptp_read_device_status(ws)
+    finite = bool(torch.isfinite(out.float()).all().item() and torch.isfinite(h.float()).all().item())
+    fl = 6.0 * cfg.M * cfg.d * cfg.F
+    value = fl / (ms * 1e-3) / 1e12
+    peak, kind = peak_for(pk, ms * n)
+    del out, h, ws
+    return {"workload": cfg.name, "M": cfg.M, "d": cfg.d, "F": cfg.F, "P": cfg.P, "chunks": cfg.chunks,
+            "variant": variant, "calls": n, "ms": ms, "tflops": value, "tokens_per_s": cfg.M / (ms * 1e-3),
+            "frac": value / peak, "peak_kind": kind, "device_status": status, "outputs_finite": finite,
+            "parity": parity}
+
+
+def leg_msweep(st, synth, dev, stream, pk, seconds=0.3):
+    """The M sweep at d=4096, F=16384, P=8, chunks=8, every M."""
+    import torch
+    res = []
+    for cfg in synth.M_SWEEP:
+        T = boundary_tensors(cfg, dev)
+        res.append(leg_boundary(st, cfg, T, dev, stream, pk, seconds=seconds,
+                                parity="tests/test_gpu_parity.py::test_m_sweep_full_size_sampled_rows "
+                                       "(sampled rows against the oracle, every variant, M = 4096/16384/65536)"))
+        del T
+        torch.cuda.empty_cache()
+    return res
+
+
+def leg_dtp(st, synth, dev, stream, pk, steps=20, warmup=3):
+    """The Delayed-TP stack: each call timed alone after an L2 flush (its
+    91 MB fit in L2), the input streams restored before the flush."""
+    import torch
+    cfg = synth.DTP_STACK
+    T = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in synth.dtp_inputs(cfg).items()}
+    xs0 = T["x_shards"].clone()
+    ws = torch.empty(st.dtp_ffn_stack_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.L, cfg.delta, st.SPTP_BF16),
+                     dtype=torch.uint8, device=dev)
+
+    def prep():  # the stack updates x_shards in place: restore the input streams
+        T["x_shards"].copy_(xs0)
+
+    def fn():
+        st.dtp_ffn_stack_forward(T["x_shards"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.L, cfg.delta, 1,
+                                 cfg.eps, workspace=ws)
+
+    def fn_with_restore():
+        prep()
+        fn()
+    flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    ms_warm = timed(fn_with_restore, steps, warmup, stream)
+    ms = timed_flushed(fn, steps, warmup, stream, flush, prep=prep)
+    del flush
+    status = st.sptp_read_device_status(ws)
+    finite = bool(torch.isfinite(T["x_shards"].float()).all().item())
+    fl = 6.0 * cfg.M * cfg.d * cfg.F * cfg.L
+    value = fl / (ms * 1e-3) / 1e12
+    return {"workload": cfg.name, "M": cfg.M, "d": cfg.d, "F": cfg.F, "P": cfg.P, "L": cfg.L, "delta": cfg.delta,
+            "variant": "auto (one fused persistent launch)", "calls": steps, "ms": ms, "tflops": value,
+            "tokens_per_s": cfg.M / (ms * 1e-3), "frac": value / pk["bf16_burst"],
+            "peak_kind": f"bf16_tflops burst ({pk['source']}): each call timed alone",
+            "frac_of_sustained": value / pk["bf16_sustained"],
+            "l2": "flushed before each call (512 MB written and read, not timed); input streams restored first",
+            "warm_back_to_back": {"ms": ms_warm, "tflops": fl / (ms_warm * 1e-3) / 1e12,
+                                  "note": "calls back to back, each with the 16.8 MB restore of x_shards"},
+            "device_status": status, "outputs_finite": finite,
+            "parity": "tests/test_gpu_parity.py::test_dtp_stack_config_full_size_sampled_rows (sampled rows "
+                      "against the oracle, flush 0 and 1, both variants)"}
+
+
+def leg_attn(st, synth, dev, stream, pk, seconds=0.3, variant="auto"):
+    """The attention-side boundary (QKV) and the row-parallel out-projection
+    at the Qwen2-7B shape."""
+    import torch
+    cfg = synth.ATTN_QWEN2_7B_SHAPE
+    T = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev) for k, v in synth.attn_inputs(cfg).items()}
+    qkv = torch.empty((cfg.P, cfg.M, cfg.N // cfg.P), dtype=torch.bfloat16, device=dev)
+    h = torch.empty_like(T["x"])
+    out = torch.empty((cfg.P, cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(st.sptp_attn_qkv_workspace_size(cfg.M, cfg.d, cfg.N, cfg.P, cfg.chunks, st.SPTP_BF16),
+                     dtype=torch.uint8, device=dev)
+    hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
+    ms_q, nq = time_calls(lambda: st.sptp_attn_qkv_forward(T["x"], T["partials"], T["gamma"], T["Wqkv"], cfg.P,
+                                                           cfg.chunks, cfg.eps, qkv_out=qkv, resid_out=h,
+                                                           workspace=ws, variant=variant), stream, seconds)
+    ms_o, no = time_calls(lambda: st.sptp_down_proj(T["attn"], T["Wo"], cfg.P, out=out, workspace=hdr), stream,
+                          seconds)
+    status = min(st.sptp_read_device_status(ws), st.sptp_read_device_status(hdr))
+    finite = bool(torch.isfinite(qkv.float()).all().item() and torch.isfinite(out.float()).all().item())
+    fq, fo = 2.0 * cfg.M * cfg.d * cfg.N, 2.0 * cfg.M * cfg.Ho * cfg.d
+    value = (fq + fo) / ((ms_q + ms_o) * 1e-3) / 1e12
+    peak, kind = peak_for(pk, ms_q * nq + ms_o * no)
+    return {"workload": cfg.name, "M": cfg.M, "d": cfg.d, "N": cfg.N, "Ho": cfg.Ho, "P": cfg.P, "chunks": cfg.chunks,
+            "variant": variant, "ms": ms_q + ms_o, "tflops": value, "frac": value / peak, "peak_kind": kind,
+            "kernels": {"qkv_boundary": {"ms": ms_q, "tflops": fq / (ms_q * 1e-3) / 1e12},
+                        "out_projection": {"ms": ms_o, "tflops": fo / (ms_o * 1e-3) / 1e12}},
+            "device_status": status, "outputs_finite": finite,
+            "parity": "tests/test_gpu_attn.py::test_attn_qkv_boundary_qwen2_7b_shape_sampled_rows and "
+                      "::test_attn_out_projection_qwen2_7b_shape_sampled_rows"}
+
+
+def leg_fp8(st, synth, dev, stream, pk, seconds=0.3):
+    """The boundary with E4M3 linear layers on the 8192 x 4096 x 14336 P=2
+    workload; the weights are quantised once, outside the timed calls."""
+    import torch
+    cfg = synth.BOUNDARY_D4096
+    T = boundary_tensors(cfg, dev)
+    M, d, F, P = cfg.M, cfg.d, cfg.F, cfg.P
+    qw = st.quantize_ffn_weights_e4m3(T["W1g"], T["W1u"], T["W2"], P)
+    out = torch.empty((P, M, d), dtype=torch.bfloat16, device=dev)
+    h = torch.empty_like(T["x"])
+    ws = torch.empty(st.sptp_ffn_fp8_workspace_size(M, d, F, P, cfg.chunks), dtype=torch.uint8, device=dev)
+    ms, n = time_calls(lambda: st.sptp_ffn_forward_fp8(T["x"], T["partials"], T["gamma"], qw, P, cfg.chunks, cfg.eps,
+                                                       out=out, resid_out=h, workspace=ws), stream, seconds)
+    status = st.sptp_read_device_status(ws)
+    finite = bool(torch.isfinite(out.float()).all().item())
+    value = 6.0 * M * d * F / (ms * 1e-3) / 1e12
+    # the fp8 peak: the measured bf16 peak times the nominal fp8 / bf16 dense
+    # ratio (4.5 / 2.25)
+    region = ms * n
+    fp8_peak = 2.0 * (pk["bf16_burst"] if region < 1000.0 else pk["bf16_sustained"])
+    return {"workload": cfg.name + "_e4m3", "M": M, "d": d, "F": F, "P": P, "chunks": cfg.chunks, "calls": n,
+            "ms": ms, "tflops": value, "frac": value / fp8_peak,
+            "peak_kind": "2 x measured bf16 %s (nominal fp8:bf16 dense ratio)" % (
+                "burst" if region < 1000.0 else "sustained"),
+            "device_status": status, "outputs_finite": finite,
+            "parity": "tests/test_gpu_fp8.py::test_boundary_fp8_d4096_full_size_sampled_rows (against the fp8 "
+                      "oracle)"}
+
+
+def configs_leg(args, st, synth, dev, stream, pk):
+    """The other workloads: the Qwen2-7B-shaped boundary and the M sweep
+    ("[Feature] Async Tensor Parallelism for Archon Engine", "Potential
+    Solution"), the Delayed-TP stack ("Affinity-Aware Sharding for Delayed
+    Tensor Parallelism", Abstract), the attention-side boundary and the
+    boundary with E4M3 linear layers.  Each is timed for about 0.3 s of
+    calls; parity on these workloads is the GPU tests' (named per entry),
+    here the device status and finite outputs are checked."""
+    import torch
+    t0 = time.perf_counter()
+    res = {}
+    cfg = synth.QWEN2_7B_SHAPE
+    T = boundary_tensors(cfg, dev)
+    res["qwen2_7b_shape"] = leg_boundary(
+        st, cfg, T, dev, stream, pk, parity="tests/test_gpu_parity.py::"
+        "test_boundary_qwen2_7b_shape_full_size_sampled_rows (sampled rows against the oracle, every variant)")
+    del T
+    torch.cuda.empty_cache()
+    res["m_sweep"] = leg_msweep(st, synth, dev, stream, pk)
+    res["dtp_stack"] = leg_dtp(st, synth, dev, stream, pk)
+    torch.cuda.empty_cache()
+    res["attention_boundary"] = leg_attn(st, synth, dev, stream, pk)
+    torch.cuda.empty_cache()
+    res["e4m3_boundary"] = leg_fp8(st, synth, dev, stream, pk)
+    torch.cuda.empty_cache()
+    res["seconds"] = time.perf_counter() - t0
+    return res
 
 
 def timed(fn, steps, warmup, stream):
@@ -532,8 +854,10 @@ def timed_flushed(fn, steps, warmup, stream, flush, prep=None):
 
 
 def run_other(args):
-    """Measurement lines for the Delayed-TP stack, the attention-side boundary
-    and the neuron-permutation gather (one GPU, device-resident inputs)."""
+    """Measurement lines for the other workloads (one GPU, device-resident
+    inputs): the Delayed-TP stack, the attention-side boundary, the neuron
+    permutation gather, the boundary with E4M3 linear layers, the M sweep and
+    the Qwen2-7B-shaped boundary."""
     import torch
     import sequence_tensor_transformer_gb300 as st
     from sequence_tensor_transformer_gb300 import synth
@@ -547,89 +871,50 @@ def run_other(args):
     line = {"n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
             "data": "synthetic", "vs_baseline": None}
     if args.workload == "dtp":
-        cfg = synth.DTP_STACK
-        inp = synth.dtp_inputs(cfg)
-        T = {k: to_dev(v) for k, v in inp.items()}
-        xs0 = T["x_shards"].clone()
-        ws = torch.empty(st.dtp_ffn_stack_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.L, cfg.delta,
-                                                         st.SPTP_BF16), dtype=torch.uint8, device=dev)
-
-        def prep():  # the stack updates x_shards in place: restore the input streams
-            T["x_shards"].copy_(xs0)
-
-        def fn():
-            st.dtp_ffn_stack_forward(T["x_shards"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.L,
-                                     cfg.delta, 1, cfg.eps, workspace=ws)
-
-        def fn_with_restore():
-            prep()
-            fn()
-        # the stack's weights and activations (91 MB) fit in L2: each call is
-        # timed alone after a flush, its inputs restored before the flush;
-        # back-to-back calls (restore included) are reported beside it
-        flush = torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
-        ms_warm = timed(fn_with_restore, args.steps, args.warmup, stream)
-        ms = timed_flushed(fn, args.steps, args.warmup, stream, flush, prep=prep)
-        del flush
-        fl = 6.0 * cfg.M * cfg.d * cfg.F * cfg.L
-        value = fl / (ms * 1e-3) / 1e12
-        line.update(metric="Delayed-TP FFN stack forward TFLOP/s", value=value, unit="TFLOP/s", ms_per_step=ms,
-                    tokens_per_s=cfg.M / (ms * 1e-3),
-                    config={"workload": cfg.name, "l2": "flushed before each call (512 MB written and read, "
-                            "not timed); value = median call; the input streams are restored before the flush"},
-                    warm_back_to_back={"ms": ms_warm, "tflops": fl / (ms_warm * 1e-3) / 1e12,
-                                       "note": "calls back to back, each with the 16.8 MB restore of x_shards"},
-                    roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                              "frac": value / pk["bf16_sustained"],
-                              "note": "whole stack: one fused launch (the default) or 3L+1 launches per call "
-                              "with SPTP_DTP_VARIANT=layers"})
+        r = leg_dtp(st, synth, dev, stream, pk, steps=args.steps, warmup=args.warmup)
+        line.update(metric="Delayed-TP FFN stack forward TFLOP/s", value=r["tflops"], unit="TFLOP/s",
+                    ms_per_step=r["ms"], tokens_per_s=r["tokens_per_s"], config={"workload": r["workload"],
+                                                                                 "l2": r["l2"]},
+                    warm_back_to_back=r["warm_back_to_back"],
+                    roofline={"bound": "tensor", "achieved": r["tflops"], "peak": pk["bf16_burst"], "unit": "TFLOP/s",
+                              "frac": r["frac"], "frac_of_sustained": r["frac_of_sustained"],
+                              "peak_kind": r["peak_kind"]})
     elif args.workload == "attn":
-        cfg = synth.ATTN_QWEN2_7B_SHAPE
-        inp = synth.attn_inputs(cfg)
-        T = {k: to_dev(v) for k, v in inp.items()}
-        qkv = torch.empty((cfg.P, cfg.M, cfg.N // cfg.P), dtype=torch.bfloat16, device=dev)
-        h = torch.empty_like(T["x"])
-        out = torch.empty((cfg.P, cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
-        ws = torch.empty(st.sptp_attn_qkv_workspace_size(cfg.M, cfg.d, cfg.N, cfg.P, cfg.chunks, st.SPTP_BF16),
-                         dtype=torch.uint8, device=dev)
-        hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
-        ms_q = timed(lambda: st.sptp_attn_qkv_forward(T["x"], T["partials"], T["gamma"], T["Wqkv"], cfg.P,
-                                                      cfg.chunks, cfg.eps, qkv_out=qkv, resid_out=h, workspace=ws),
-                     args.steps, args.warmup, stream)
-        ms_o = timed(lambda: st.sptp_down_proj(T["attn"], T["Wo"], cfg.P, out=out, workspace=hdr), args.steps,
-                     args.warmup, stream)
-        fq, fo = 2.0 * cfg.M * cfg.d * cfg.N, 2.0 * cfg.M * cfg.Ho * cfg.d
-        value = (fq + fo) / ((ms_q + ms_o) * 1e-3) / 1e12
+        r = leg_attn(st, synth, dev, stream, pk, seconds=max(0.3, args.steps * 0.7e-3), variant=args.variant)
         line.update(metric="attention-side boundary (QKV boundary + row-parallel out-projection) TFLOP/s",
-                    value=value, unit="TFLOP/s", ms_per_step=ms_q + ms_o,
-                    config={"workload": cfg.name, "l2": "inputs larger than L2 (QKV boundary 587 MB, "
-                            "out-projection 143 MB read per call)"},
-                    kernels={"qkv_boundary": {"ms": ms_q, "achieved": fq / (ms_q * 1e-3) / 1e12},
-                             "out_projection": {"ms": ms_o, "achieved": fo / (ms_o * 1e-3) / 1e12}},
-                    roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                              "frac": value / pk["bf16_sustained"]})
+                    value=r["tflops"], unit="TFLOP/s", ms_per_step=r["ms"],
+                    config={"workload": r["workload"], "variant": args.variant,
+                            "l2": "inputs larger than L2 (QKV boundary 587 MB, out-projection 143 MB read per call)"},
+                    kernels=r["kernels"],
+                    roofline={"bound": "tensor", "achieved": r["tflops"], "unit": "TFLOP/s", "frac": r["frac"],
+                              "peak_kind": r["peak_kind"]})
     elif args.workload == "fp8":
         line.update(_fp8_line(args, synth.BOUNDARY_D4096, to_dev, dev, stream, pk))
     elif args.workload in ("msweep", "qwen2"):
-        cfgs = synth.M_SWEEP if args.workload == "msweep" else (synth.QWEN2_7B_SHAPE,)
-        per = [_boundary_timing(cfg, args, to_dev, dev, stream, pk) for cfg in cfgs]
-        fl = sum(r["flops"] for r in per)
+        if args.workload == "msweep":
+            per = leg_msweep(st, synth, dev, stream, pk, seconds=1.0)
+            name = "M sweep 4096..65536 (d=4096, F=16384, P=8, chunks=8)"
+        else:
+            cfg = synth.QWEN2_7B_SHAPE
+            per = [leg_boundary(st, cfg, boundary_tensors(cfg, dev), dev, stream, pk, variant=args.variant,
+                                seconds=1.0)]
+            name = cfg.name
+        fl = sum(6.0 * r["M"] * r["d"] * r["F"] for r in per)
         ms = sum(r["ms"] for r in per)
         value = fl / (ms * 1e-3) / 1e12
-        name = "M sweep 4096..65536 (d=4096, F=16384, P=8, chunks=8)" if args.workload == "msweep" else cfgs[0].name
         # the oracle on a fixed 512-row sample (per-row work is the same at every M of the sweep)
-        ccfg = cfgs[0]
-        csec = oracle_rate(ccfg, min(512, ccfg.M))
+        ccfg = synth.M_SWEEP[0] if args.workload == "msweep" else synth.QWEN2_7B_SHAPE
         rows = min(512, ccfg.M)
+        csec = oracle_rate(ccfg, rows)
         cpu = {"value": 6.0 * rows * ccfg.d * ccfg.F / csec / 1e12, "unit": "TFLOP/s", "tokens_per_s": rows / csec,
                "cores": cores(), "kind": "oracle",
                "sample": f"first {rows} token rows of {ccfg.name}, float64 numpy oracle, {csec:.2f} s"}
         line.update(metric="SP-TP FFN forward TFLOP/s & tokens/s, % of roofline: " + name, value=value,
                     unit="TFLOP/s", ms_per_step=ms, config={"workload": name, "l2": "inputs larger than L2"},
-                    cpu_baseline=cpu,
-                    per_config=[{k: v for k, v in r.items() if k != "flops"} for r in per],
-                    roofline={"bound": "tensor", "achieved": value, "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                    cpu_baseline=cpu, per_config=per,
+                    roofline={"bound": "tensor", "achieved": value, "unit": "TFLOP/s",
                               "frac": value / pk["bf16_sustained"],
+                              "peak_kind": f"bf16_tflops_sustained ({pk['source']}): about 1 s of calls per config",
                               "note": "one call of every config, flops over summed time; per-config figures beside"})
     else:
         cfg = synth.DTP_STACK
@@ -661,37 +946,6 @@ def run_other(args):
                               "frac": gbs / pk["hbm"], "algorithmic_bytes": by})
     print(json.dumps(line), flush=True)
     return 0
-
-
-def _boundary_timing(cfg, args, to_dev, dev, stream, pk):
-    """Times sptp_ffn_forward on one boundary config (device-resident inputs,
-    about 0.3 s of calls after warm-up)."""
-    import torch
-    import sequence_tensor_transformer_gb300 as st
-    from sequence_tensor_transformer_gb300 import synth
-
-    inp = synth.boundary_inputs(cfg)
-    T = {k: to_dev(v) for k, v in inp.items()}
-    del inp
-    out = torch.empty((cfg.P, cfg.M, cfg.d), dtype=torch.bfloat16, device=dev)
-    h = torch.empty_like(T["x"])
-    ws = torch.empty(st.sptp_ffn_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.chunks, st.SPTP_BF16),
-                     dtype=torch.uint8, device=dev)
-
-    def fn():
-        st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.chunks,
-                            cfg.eps, out=out, resid_out=h, workspace=ws)
-    fl = 6.0 * cfg.M * cfg.d * cfg.F
-    est_ms = fl / 1.6e15 * 1e3
-    steps = max(10, int(300.0 / est_ms))
-    ms = timed(fn, steps, max(3, min(args.warmup, 20)), stream)
-    assert st.sptp_read_device_status(ws) == 0
-    value = fl / (ms * 1e-3) / 1e12
-    del T, out, h, ws
-    torch.cuda.empty_cache()
-    return {"workload": cfg.name, "M": cfg.M, "d": cfg.d, "F": cfg.F, "P": cfg.P, "chunks": cfg.chunks,
-            "steps": steps, "ms": ms, "tflops": value, "tokens_per_s": cfg.M / (ms * 1e-3),
-            "frac_sustained": value / pk["bf16_sustained"], "flops": fl}
 
 
 def _fp8_line(args, cfg, to_dev, dev, stream, pk):

@@ -45,9 +45,19 @@
 extern "C" {
 #endif
 
-typedef enum { SPTP_BF16 = 0, SPTP_FP32 = 1 } sptp_dtype;
+/* In C++ the enums get int as their underlying type, so that every int a C
+ * caller passes is a valid value (and is rejected by the checks below rather
+ * than being undefined). */
+#ifdef __cplusplus
+#define SPTP_ENUM_INT : int
+#else
+#define SPTP_ENUM_INT
+#endif
 
-typedef enum {
+/* Element type of activations, gamma and weights. */
+typedef enum sptp_dtype_e SPTP_ENUM_INT { SPTP_BF16 = 0, SPTP_FP32 = 1 } sptp_dtype;
+
+typedef enum sptp_status_e SPTP_ENUM_INT {
     SPTP_OK = 0,
     SPTP_ERR_NULL = -1,          /* a required pointer is NULL */
     SPTP_ERR_SHAPE = -2,         /* a size or divisibility rule is violated */
@@ -55,17 +65,53 @@ typedef enum {
     SPTP_ERR_WORKSPACE = -4,     /* ws_bytes smaller than the *_workspace_size query */
     SPTP_ERR_CUDA = -5,          /* a CUDA runtime call or kernel launch failed */
     SPTP_ERR_TIMEOUT = -6,       /* a bounded device-side wait ran out */
-    SPTP_ERR_DEVICE = -7,        /* current device is not compute capability 10.3 */
+    SPTP_ERR_UNIMPLEMENTED = -7, /* the requested variant does not exist for this entry point and
+                                    dtype, or this device cannot run its launch */
     SPTP_ERR_ALIAS = -8,         /* an output overlaps an input it must not overlap */
-    SPTP_ERR_TOO_LARGE = -9      /* the problem needs more scratch than the library's static array */
+    SPTP_ERR_TOO_LARGE = -9,     /* the problem needs more scratch than the library's static array */
+    SPTP_ERR_DEVICE = -10,       /* current device is not compute capability 10.3 */
+    SPTP_ERR_BOUNDS = -11        /* bounds-checked builds only: a kernel computed an index or address
+                                    outside its buffer and skipped the access */
 } sptp_status;
+
+/*
+ * sptp_variant -- how a boundary call is split into launches.  Every
+ * variant computes the same outputs; they differ in how the partial sum +
+ * residual + RMSNorm rows reach the GEMMs.  SPTP_VARIANT_AUTO is the
+ * library's default for the entry point and dtype; any other value runs
+ * exactly that variant or returns SPTP_ERR_UNIMPLEMENTED (nothing enqueued)
+ * where it does not exist or this device cannot co-schedule its launch.
+ *   PAIR    (sptp_ffn_forward, sptp_attn_qkv_forward; bf16 and fp32) the
+ *           prologue kernel over all M rows, then the GEMM launches (bf16:
+ *           tcgen05 CTA-pair GEMMs; fp32: CUDA-core GEMMs).  The default.
+ *   CHAIN   (sptp_ffn_forward, bf16) the prologue kernel, then ONE persistent
+ *           launch running every gate/up tile and then every down tile; a
+ *           down tile starts as soon as the gate/up tiles of its rows are
+ *           stored.
+ *   FUSED   (sptp_ffn_forward, sptp_attn_qkv_forward, dtp_ffn_stack_forward;
+ *           bf16) ONE persistent launch: prologue warps produce the normed
+ *           rows in sequence order, 256-row block by block, and the GEMM tiles
+ *           consume each block as soon as it is published (the chunked
+ *           all-gather + matmul of [A] "Potential Solution", literally).  The
+ *           default of dtp_ffn_stack_forward for bf16.
+ *   LAYERS  (dtp_ffn_stack_forward) a prologue launch and two GEMM launches
+ *           per module.  The default for fp32, and for bf16 where FUSED
+ *           cannot be launched.
+ */
+typedef enum sptp_variant_e SPTP_ENUM_INT {
+    SPTP_VARIANT_AUTO = 0,
+    SPTP_VARIANT_PAIR = 1,
+    SPTP_VARIANT_CHAIN = 2,
+    SPTP_VARIANT_FUSED = 3,
+    SPTP_VARIANT_LAYERS = 4
+} sptp_variant;
 
 /* Bytes at the start of every workspace holding the device status words. */
 #define SPTP_WS_HEADER_BYTES 4096
 
 /* Workspace bytes needed by sptp_ffn_forward for these sizes (0 on bad args).
  * Layout: header | y [M][d] normed activations | s [P][M][F/P] SwiGLU output. */
-size_t sptp_ffn_workspace_size(int M, int d, int F, int P, int chunks, int dtype);
+size_t sptp_ffn_workspace_size(int M, int d, int F, int P, int chunks, sptp_dtype dtype);
 
 /*
  * sptp_ffn_forward -- one SP-TP FFN sub-layer boundary ([A] "Potential
@@ -83,27 +129,39 @@ size_t sptp_ffn_workspace_size(int M, int d, int F, int P, int chunks, int dtype
  *   partials  [P][M][d] the previous sub-layer's row-parallel partials
  *   gamma     [d]       RMSNorm scale
  *   W1g, W1u  [F][d]    gate / up projections;  W2 [d][F] down projection
- *   chunks    number of sequence chunks; M % chunks == 0, chunks % P == 0.
- *             Chunk c belongs to shard floor(c*P/chunks); the GEMMs consume
- *             chunks in order.
+ *   chunks    number of sequence chunks of the all-gather; M % chunks == 0,
+ *             chunks % P == 0.  Chunk c is rows [c*M/chunks, (c+1)*M/chunks)
+ *             and belongs to shard floor(c*P/chunks).  With
+ *             SPTP_VARIANT_FUSED the gate/up tiles read a chunk's rows of y as
+ *             soon as every row of the chunk is produced; the PAIR and CHAIN
+ *             variants produce every chunk before the GEMMs start, so for
+ *             them chunks changes nothing but the validation.
  *   out       [P][M][d] the next sub-layer's P partials (not reduced).  Must
  *             not overlap any input or the workspace.
  *   resid_out [M][d]    h, the new residual stream; may be NULL (not written)
  *             and may be exactly x (in place).
  *   workspace at least sptp_ffn_workspace_size(...) bytes, 256-byte aligned.
  * Numerics (bf16): sums, norm and SwiGLU in fp32; h, y, s and out are each
- * rounded once to bf16 (round to nearest even).
+ * rounded once to bf16 (round to nearest even).  Every variant gives the same
+ * bits.
+ * sptp_ffn_forward runs SPTP_VARIANT_AUTO; sptp_ffn_forward_ex runs the
+ * variant it is given (PAIR, CHAIN or FUSED; see sptp_variant).
  */
 int sptp_ffn_forward(const void* x, const void* partials, const void* gamma,
                      const void* W1g, const void* W1u, const void* W2,
-                     int M, int d, int F, int P, int chunks, float eps, int dtype,
+                     int M, int d, int F, int P, int chunks, float eps, sptp_dtype dtype,
                      void* out, void* resid_out,
                      void* workspace, size_t ws_bytes, void* cuda_stream);
+int sptp_ffn_forward_ex(const void* x, const void* partials, const void* gamma,
+                        const void* W1g, const void* W1u, const void* W2,
+                        int M, int d, int F, int P, int chunks, float eps, sptp_dtype dtype,
+                        void* out, void* resid_out,
+                        void* workspace, size_t ws_bytes, void* cuda_stream, sptp_variant variant);
 
 /* Workspace bytes needed by dtp_ffn_stack_forward (0 on bad args).
  * Layout: header | y [P][M][d] | s [P][M][F/P] | pending ring [S][P][M][d],
  * S = min(delta + 1, L). */
-size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta, int dtype);
+size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta, sptp_dtype dtype);
 
 /*
  * dtp_ffn_stack_forward -- a Delayed-TP stack of L FFN sub-layers ([B],
@@ -120,12 +178,20 @@ size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta
  *   delta >= 0; L >= 1; 1 + (P-1)*min(L, delta+1) <= 64.
  * Numerics (bf16): each stream update is summed in fp32 (own partial first,
  * then other shards in ascending shard order, then x_p) and rounded to bf16.
+ * dtp_ffn_stack_forward runs SPTP_VARIANT_AUTO (FUSED for bf16 where the
+ * device can run it, else LAYERS); dtp_ffn_stack_forward_ex runs the variant
+ * it is given (FUSED or LAYERS).
  */
 int dtp_ffn_stack_forward(void* x_shards, const void* gamma,
                           const void* W1g, const void* W1u, const void* W2,
                           int M, int d, int F, int P, int L, int delta, int flush,
-                          float eps, int dtype,
+                          float eps, sptp_dtype dtype,
                           void* workspace, size_t ws_bytes, void* cuda_stream);
+int dtp_ffn_stack_forward_ex(void* x_shards, const void* gamma,
+                             const void* W1g, const void* W1u, const void* W2,
+                             int M, int d, int F, int P, int L, int delta, int flush,
+                             float eps, sptp_dtype dtype,
+                             void* workspace, size_t ws_bytes, void* cuda_stream, sptp_variant variant);
 
 /* ---- Step-level entry points (the same kernels the two calls above use). ---- */
 
@@ -135,7 +201,7 @@ int dtp_ffn_stack_forward(void* x_shards, const void* gamma,
  * y_out [M][d] must not overlap the inputs.
  */
 int sptp_prologue(const void* x, const void* partials, const void* gamma,
-                  int M, int d, int P, float eps, int dtype,
+                  int M, int d, int P, float eps, sptp_dtype dtype,
                   void* h_out, void* y_out, void* cuda_stream);
 
 /*
@@ -145,7 +211,7 @@ int sptp_prologue(const void* x, const void* partials, const void* gamma,
  * SPTP_WS_HEADER_BYTES (status words).
  */
 int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u,
-                       int M, int d, int F, int P, int dtype, void* s_out,
+                       int M, int d, int F, int P, sptp_dtype dtype, void* s_out,
                        void* workspace, size_t ws_bytes, void* cuda_stream);
 
 /*
@@ -155,12 +221,12 @@ int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u,
  * per-shard attention output, W2 = Wo [d][F]).  workspace: at least
  * SPTP_WS_HEADER_BYTES.
  */
-int sptp_down_proj(const void* s, const void* W2, int M, int d, int F, int P, int dtype,
+int sptp_down_proj(const void* s, const void* W2, int M, int d, int F, int P, sptp_dtype dtype,
                    void* out, void* workspace, size_t ws_bytes, void* cuda_stream);
 
 /* Workspace bytes needed by sptp_attn_qkv_forward (0 on bad args).
  * Layout: header | y [M][d]. */
-size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, int dtype);
+size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, sptp_dtype dtype);
 
 /*
  * sptp_attn_qkv_forward -- the sub-layer boundary in front of an attention
@@ -176,11 +242,17 @@ size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, int 
  * The row-parallel output projection after attention, which yields the next
  * P partials, is sptp_down_proj with F = the attention width (attn [P][M][F/P],
  * Wo [d][F]).
+ * sptp_attn_qkv_forward runs SPTP_VARIANT_AUTO (PAIR); sptp_attn_qkv_forward_ex
+ * runs the variant it is given (PAIR, or FUSED for bf16).
  */
 int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma, const void* Wqkv,
-                          int M, int d, int N, int P, int chunks, float eps, int dtype,
+                          int M, int d, int N, int P, int chunks, float eps, sptp_dtype dtype,
                           void* qkv_out, void* resid_out,
                           void* workspace, size_t ws_bytes, void* cuda_stream);
+int sptp_attn_qkv_forward_ex(const void* x, const void* partials, const void* gamma, const void* Wqkv,
+                             int M, int d, int N, int P, int chunks, float eps, sptp_dtype dtype,
+                             void* qkv_out, void* resid_out,
+                             void* workspace, size_t ws_bytes, void* cuda_stream, sptp_variant variant);
 
 /*
  * sptp_permute_ffn_neurons -- executes a neuron-permutation shard map for
@@ -200,7 +272,7 @@ int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma
  *   200 KiB.  workspace: at least SPTP_WS_HEADER_BYTES.
  */
 int sptp_permute_ffn_neurons(const void* W1g, const void* W1u, const void* W2, const int* perm,
-                             int L, int d, int F, int dtype,
+                             int L, int d, int F, sptp_dtype dtype,
                              void* W1g_out, void* W1u_out, void* W2_out,
                              void* workspace, size_t ws_bytes, void* cuda_stream);
 
@@ -311,28 +383,41 @@ int sptp_wait_selftest(void* workspace, size_t ws_bytes, unsigned long long limi
  * owns every device allocation, or a serving loop that must not call
  * cudaMalloc because it can synchronise the device).  The pages describe no
  * such entry point; it exists for those callers.
- *   - Arguments, results and errors are those of sptp_ffn_forward, without
- *     the workspace.  The caller still passes every input and output.
+ *   - Arguments, results and errors are those of sptp_ffn_forward (variant
+ *     AUTO), without the workspace.  The caller still passes every input and
+ *     output.  The arguments are checked first, in the same order and with
+ *     the same codes; then the size limit; then the device.
  *   - Scratch is a library-owned 256-byte aligned __device__ array of
  *     SPTP_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU loading the library
  *     holds until the process exits.  Problems whose
  *     sptp_ffn_workspace_size(...) exceeds it return SPTP_ERR_TOO_LARGE
  *     before any CUDA call (bf16, d=4096, F=14336: up to about 1800 tokens).
- *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
- *     call on a device looks up the array's device address (once per device,
- *     with that device current); make that first call before any stream
- *     capture.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The array's
+ *     device address is looked up (cudaGetSymbolAddress) on the first call in
+ *     each device context, with that device current; make that first call
+ *     before any stream capture.
  *   - Every call shares the one array, so calls whose work overlaps on the
  *     GPU (different streams, or different host threads) race and give wrong
  *     results; serialise them.  The array keeps the last call's contents; the
  *     status words are cleared at the start of each call.
- *   - sptp_read_device_status does not apply (its status words live in the
- *     shared array).
  */
 int sptp_ffn_forward_noalloc(const void* x, const void* partials, const void* gamma,
                              const void* W1g, const void* W1u, const void* W2,
-                             int M, int d, int F, int P, int chunks, float eps, int dtype,
+                             int M, int d, int F, int P, int chunks, float eps, sptp_dtype dtype,
                              void* out, void* resid_out, void* cuda_stream);
+
+/*
+ * Failure detection of the no-allocation forward, whose status words live in
+ * the library's static array rather than in a caller workspace.
+ *   sptp_noalloc_read_device_status: as sptp_read_device_status, for the
+ *     last sptp_ffn_forward_noalloc on the current device (synchronises
+ *     `cuda_stream`).
+ *   sptp_noalloc_wait_selftest: as sptp_wait_selftest, with the static
+ *     array's status words.
+ * No counterpart on the pages.
+ */
+int sptp_noalloc_read_device_status(void* cuda_stream);
+int sptp_noalloc_wait_selftest(unsigned long long limit_ns, int preset_flag, void* cuda_stream);
 
 /* Human-readable text of a status code (static storage). */
 const char* sptp_status_string(int status);

@@ -20,13 +20,19 @@ __all__ = [
     "sptp_ffn_forward_noalloc", "SPTP_NOALLOC_SCRATCH_BYTES", "sptp_permute_ffn_neurons",
     "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward", "sptp_quantize_rows_e4m3",
     "quantize_ffn_weights_e4m3", "sptp_ffn_fp8_workspace_size", "sptp_ffn_forward_fp8",
-    "sptp_gateup_swiglu_e4m3", "sptp_down_proj_e4m3", "sptp_prologue_e4m3",
+    "sptp_gateup_swiglu_e4m3", "sptp_down_proj_e4m3", "sptp_prologue_e4m3", "VARIANTS", "STATUS",
+    "sptp_noalloc_read_device_status", "sptp_noalloc_wait_selftest",
 ]
 
 SPTP_BF16 = 0
 SPTP_FP32 = 1
 SPTP_WS_HEADER_BYTES = 4096
 SPTP_NOALLOC_SCRATCH_BYTES = 64 << 20
+# sptp_variant: how a boundary call is split into launches (include/sptp.h)
+VARIANTS = {"auto": 0, "pair": 1, "chain": 2, "fused": 3, "layers": 4}
+# sptp_status codes
+STATUS = {"ok": 0, "null": -1, "shape": -2, "dtype": -3, "workspace": -4, "cuda": -5, "timeout": -6,
+          "unimplemented": -7, "alias": -8, "too_large": -9, "device": -10, "bounds": -11}
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsptp.so")
 
 EXPORTED_SYMBOLS = (
@@ -35,7 +41,8 @@ EXPORTED_SYMBOLS = (
     "sptp_read_device_status", "sptp_wait_selftest", "sptp_status_string", "sptp_ffn_forward_noalloc",
     "sptp_permute_ffn_neurons", "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward",
     "sptp_quantize_rows_e4m3", "sptp_ffn_fp8_workspace_size", "sptp_ffn_forward_fp8", "sptp_gateup_swiglu_e4m3",
-    "sptp_down_proj_e4m3", "sptp_prologue_e4m3",
+    "sptp_down_proj_e4m3", "sptp_prologue_e4m3", "sptp_ffn_forward_ex", "dtp_ffn_stack_forward_ex",
+    "sptp_attn_qkv_forward_ex", "sptp_noalloc_read_device_status", "sptp_noalloc_wait_selftest",
 )
 
 _lib = None
@@ -64,6 +71,11 @@ _SIGS = {
     "sptp_gateup_swiglu_e4m3": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "sptp_down_proj_e4m3": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "sptp_prologue_e4m3": (_I, [_P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "sptp_ffn_forward_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _Z, _P, _I]),
+    "dtp_ffn_stack_forward_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P, _I]),
+    "sptp_attn_qkv_forward_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _Z, _P, _I]),
+    "sptp_noalloc_read_device_status": (_I, [_P]),
+    "sptp_noalloc_wait_selftest": (_I, [_U64, _I, _P]),
 }
 
 
@@ -132,10 +144,29 @@ def _expect(name, t, shape, dtype, optional=False):
 
 
 def _same_device(*ts):
+    """Every tensor argument on one CUDA device, the current one: the library
+    launches on the current device and takes its stream, scratch and device
+    properties from it, so a tensor elsewhere would be handed to kernels of
+    another device.  Checked before any pointer reaches the C ABI."""
     ts = [t for t in ts if t is not None]
     for t in ts[1:]:
         if t.device != ts[0].device:
             raise ValueError(f"tensors on {ts[0].device} and {t.device}: one device expected")
+    if ts and ts[0].device.type != "cuda":
+        raise ValueError("device tensors only")
+    if ts:
+        cur = torch.cuda.current_device()
+        if ts[0].device.index != cur:
+            raise ValueError(f"tensors on {ts[0].device} but the current device is cuda:{cur}: "
+                             f"call torch.cuda.set_device({ts[0].device.index}) first")
+
+
+def _variant(v) -> int:
+    if isinstance(v, str):
+        if v not in VARIANTS:
+            raise ValueError(f"unknown variant {v!r}; one of {sorted(VARIANTS)}")
+        return VARIANTS[v]
+    return int(v)
 
 
 def _nbytes(t) -> int:
@@ -143,8 +174,11 @@ def _nbytes(t) -> int:
 
 
 def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if stream.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream on {stream.device} but the current device is cuda:{torch.cuda.current_device()}")
+    return stream.cuda_stream
 
 
 def _check(fn: str, code: int):
@@ -181,8 +215,9 @@ def _check_ffn_args(x, partials, gamma, W1g, W1u, W2, P, out, resid_out, dtype=N
 
 
 def sptp_ffn_forward(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, out=None, resid_out=None,
-                     workspace=None, stream=None, write_resid=True):
-    """SP-TP FFN boundary.  Returns (out [P,M,d], resid_out [M,d] or None)."""
+                     workspace=None, stream=None, write_resid=True, variant="auto"):
+    """SP-TP FFN boundary.  Returns (out [P,M,d], resid_out [M,d] or None).
+    variant: "auto" (the library's default), "pair", "chain" or "fused"."""
     M, d = x.shape
     F = W1g.shape[0]
     dt = _dtype_code(x)
@@ -194,16 +229,18 @@ def sptp_ffn_forward(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, out=None,
     if workspace is None:
         workspace = _workspace(sptp_ffn_workspace_size(M, d, F, P, chunks, dt), x.device)
     _same_device(x, workspace)
-    code = lib().sptp_ffn_forward(
+    code = lib().sptp_ffn_forward_ex(
         _ptr(x), _ptr(partials), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, chunks,
-        float(eps), dt, _ptr(out), _ptr(resid_out), _ptr(workspace), _nbytes(workspace), _stream(stream))
+        float(eps), dt, _ptr(out), _ptr(resid_out), _ptr(workspace), _nbytes(workspace), _stream(stream),
+        _variant(variant))
     _check("sptp_ffn_forward", code)
     return out, resid_out
 
 
 def dtp_ffn_stack_forward(x_shards, gamma, W1g, W1u, W2, P, L, delta, flush, eps, workspace=None,
-                          stream=None):
-    """Delayed-TP stack; updates x_shards [P,M,d] in place and returns it."""
+                          stream=None, variant="auto"):
+    """Delayed-TP stack; updates x_shards [P,M,d] in place and returns it.
+    variant: "auto" (the library's default), "fused" or "layers"."""
     _, M, d = x_shards.shape
     F = W1g.shape[1]
     dt = _dtype_code(x_shards)
@@ -215,9 +252,9 @@ def dtp_ffn_stack_forward(x_shards, gamma, W1g, W1u, W2, P, L, delta, flush, eps
     if workspace is None:
         workspace = _workspace(dtp_ffn_stack_workspace_size(M, d, F, P, L, delta, dt), x_shards.device)
     _same_device(x_shards, gamma, W1g, W1u, W2, workspace)
-    code = lib().dtp_ffn_stack_forward(
+    code = lib().dtp_ffn_stack_forward_ex(
         _ptr(x_shards), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, L, delta, int(flush),
-        float(eps), dt, _ptr(workspace), _nbytes(workspace), _stream(stream))
+        float(eps), dt, _ptr(workspace), _nbytes(workspace), _stream(stream), _variant(variant))
     _check("dtp_ffn_stack_forward", code)
     return x_shards
 
@@ -280,8 +317,8 @@ def sptp_ffn_forward_noalloc(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, o
     device allocation inside the call; the caller passes out/resid_out)."""
     M, d = x.shape
     F = W1g.shape[0]
-    _check_ffn_args(x, partials, gamma, W1g, W1u, W2, P, out, resid_out)
     _expect("out", out, (P, M, d), x.dtype)
+    _check_ffn_args(x, partials, gamma, W1g, W1u, W2, P, out, resid_out)
     code = lib().sptp_ffn_forward_noalloc(
         _ptr(x), _ptr(partials), _ptr(gamma), _ptr(W1g), _ptr(W1u), _ptr(W2), M, d, F, P, chunks, float(eps),
         _dtype_code(x), _ptr(out), _ptr(resid_out), _stream(stream))
@@ -289,13 +326,23 @@ def sptp_ffn_forward_noalloc(x, partials, gamma, W1g, W1u, W2, P, chunks, eps, o
     return out, resid_out
 
 
+def sptp_noalloc_read_device_status(stream=None) -> int:
+    """Status words of the last no-allocation forward on the current device."""
+    return int(lib().sptp_noalloc_read_device_status(_stream(stream)))
+
+
+def sptp_noalloc_wait_selftest(limit_ns: int, preset_flag: bool, stream=None) -> int:
+    return int(lib().sptp_noalloc_wait_selftest(int(limit_ns), int(preset_flag), _stream(stream)))
+
+
 def sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dtype=SPTP_BF16) -> int:
     return int(lib().sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dtype))
 
 
 def sptp_attn_qkv_forward(x, partials, gamma, Wqkv, P, chunks, eps, qkv_out=None, resid_out=None,
-                          workspace=None, stream=None, write_resid=True):
-    """Boundary in front of attention: returns (qkv [P,M,N/P], resid_out)."""
+                          workspace=None, stream=None, write_resid=True, variant="auto"):
+    """Boundary in front of attention: returns (qkv [P,M,N/P], resid_out).
+    variant: "auto" (the library's default), "pair" or "fused"."""
     M, d = x.shape
     N = Wqkv.shape[0]
     dt = _dtype_code(x)
@@ -311,9 +358,9 @@ def sptp_attn_qkv_forward(x, partials, gamma, Wqkv, P, chunks, eps, qkv_out=None
         resid_out = torch.empty_like(x)
     if workspace is None:
         workspace = _workspace(sptp_attn_qkv_workspace_size(M, d, N, P, chunks, dt), x.device)
-    code = lib().sptp_attn_qkv_forward(_ptr(x), _ptr(partials), _ptr(gamma), _ptr(Wqkv), M, d, N, P, chunks,
-                                       float(eps), dt, _ptr(qkv_out), _ptr(resid_out), _ptr(workspace),
-                                       _nbytes(workspace), _stream(stream))
+    code = lib().sptp_attn_qkv_forward_ex(_ptr(x), _ptr(partials), _ptr(gamma), _ptr(Wqkv), M, d, N, P, chunks,
+                                          float(eps), dt, _ptr(qkv_out), _ptr(resid_out), _ptr(workspace),
+                                          _nbytes(workspace), _stream(stream), _variant(variant))
     _check("sptp_attn_qkv_forward", code)
     return qkv_out, resid_out
 
@@ -337,10 +384,12 @@ def sptp_permute_ffn_neurons(W1g, W1u, W2, perm, workspace=None, stream=None):
 
 
 def sptp_read_device_status(workspace, stream=None) -> int:
+    _same_device(workspace)
     return int(lib().sptp_read_device_status(_ptr(workspace), _stream(stream)))
 
 
 def sptp_wait_selftest(workspace, limit_ns: int, preset_flag: bool, stream=None) -> int:
+    _same_device(workspace)
     return int(lib().sptp_wait_selftest(_ptr(workspace), _nbytes(workspace), int(limit_ns), int(preset_flag),
                                         _stream(stream)))
 

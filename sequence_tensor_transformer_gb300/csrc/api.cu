@@ -80,38 +80,34 @@ size_t dtp_counter_bytes(int M, int P, int L) {
     return static_cast<size_t>(L) * mt * (2 + static_cast<size_t>(P)) * sizeof(int);
 }
 
-// Delayed-TP execution: one fused persistent launch for the whole stack
-// (bf16; the default) or, with SPTP_DTP_VARIANT=layers, a prologue and two
-// GEMM launches per module.
-bool dtp_fused_selected() {
-    const char* v = std::getenv("SPTP_DTP_VARIANT");
-    return !(v != nullptr && std::strcmp(v, "layers") == 0);
+// A variant value the header defines (sptp_variant).
+bool variant_known(int v) { return v >= SPTP_VARIANT_AUTO && v <= SPTP_VARIANT_LAYERS; }
+
+// A cooperative launch the runtime refuses to start enqueues nothing; the
+// caller may take another path (SPTP_VARIANT_AUTO) or report it.
+bool launch_rejected(cudaError_t e) {
+    return e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidValue || e == cudaErrorNotSupported ||
+           e == cudaErrorInvalidConfiguration;
 }
 
-// With SPTP_STRICT_VARIANT=1 a selected fused launch that cannot run is an
-// error (SPTP_ERR_CUDA) instead of a fall-back to the multi-launch path; the
-// tests use it to make sure the variant they name is the one that ran.
-// The attention-side boundary as one fused launch: SPTP_ATTN_VARIANT=fused
-// (else prologue + column-parallel GEMM).
-bool attn_fused_selected() {
-    const char* v = std::getenv("SPTP_ATTN_VARIANT");
-    return v != nullptr && std::strcmp(v, "fused") == 0;
-}
-
-bool strict_variant() {
-    const char* v = std::getenv("SPTP_STRICT_VARIANT");
-    return v != nullptr && std::strcmp(v, "1") == 0;
-}
-
-// Readiness counters of the fused boundary: per 256-row block, prologue rows
-// done; per (shard, 256-row block), gate/up tile halves stored.
-size_t fused_counter_bytes(int M, int P) {
+// Readiness counters of the fused boundary: per sequence chunk, prologue rows
+// published; per (shard, 256-row block), gate/up tile halves stored.
+size_t fused_counter_bytes(int M, int P, int chunks) {
     const size_t mt = (static_cast<size_t>(M) + 255) / 256;
-    return (mt + static_cast<size_t>(P) * mt) * sizeof(int);
+    return (static_cast<size_t>(chunks) + static_cast<size_t>(P) * mt) * sizeof(int);
 }
 
+// Whether the persistent launches can run here: 0 if every CTA pair of the
+// launch cannot be resident at once (the CTAs wait on one another).
+bool fused_runs(const DevInfo& di, int M, int chunks) {
+    // a chunk's counter reaches rows x prologue warps (32-bit)
+    return static_cast<long long>(M / chunks) * 8 < (1ll << 31) && fused_max_pairs(di.sms) > 0;
+}
+bool dtp_fused_runs(const DevInfo& di, int M, int P, int L) {
+    // the kernel numbers prologue rows with 32 bits
+    return static_cast<long long>(P) * M * (L + 1) < (1ll << 31) && dtp_fused_max_pairs(di.sms) > 0;
+}
 
-constexpr int SPTP_ERR_UNSUPPORTED = -100;  // internal: fused path not available here
 constexpr int kFirstBandRows = 2048;
 
 // ------------------------------------------------------------ fp8 (E4M3)
@@ -142,21 +138,16 @@ Fp8Layout fp8_layout(int M, int d, int F, int P) {
     return L;
 }
 
-// The whole bf16 boundary as one persistent launch (fused.cu).  Returns
-// SPTP_ERR_UNSUPPORTED, having enqueued nothing, where it cannot launch.
+// The whole bf16 boundary as one persistent launch (fused.cu), or with
+// pre_normed its GEMM tiles alone after a prologue launch (the CHAIN
+// variant).  The caller has checked fused_runs().  Returns SPTP_OK, or
+// SPTP_ERR_UNIMPLEMENTED if the runtime refused the launch (nothing but the
+// counter reset enqueued), or SPTP_ERR_CUDA.
 int fused_forward(const void* x, const void* partials, const void* gamma, const void* W1g, const void* W1u,
                   const void* W2, int M, int d, int F, int P, int chunks, float eps, void* out, void* resid_out,
                   void* y, void* sbuf, int* counters, DeviceStatus* st, int band, const DevInfo& di,
                   cudaStream_t s, bool pre_normed = false) {
-    static bool unavailable[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (unavailable[dev & 63]) return SPTP_ERR_UNSUPPORTED;
     const int max_pairs = fused_max_pairs(di.sms);
-    if (max_pairs <= 0) {
-        unavailable[dev & 63] = true;
-        return SPTP_ERR_UNSUPPORTED;
-    }
     const size_t es = 2;
     const int f = F / P;
     const size_t act = static_cast<size_t>(M) * d * es;
@@ -205,42 +196,28 @@ int fused_forward(const void* x, const void* partials, const void* gamma, const 
     p.tiles_dn = P * p.mt * p.nt_dn;
     p.block_rows = P + 1 <= 5 && d <= 4096 ? 1 : 0;
     p.pre_normed = pre_normed ? 1 : 0;
-    p.rb_ready = counters;
-    p.gu_done = counters + p.mt;
+    p.chunks = chunks;
+    p.chunk_rows = chunk_rows;
+    p.chunk_ready = counters;
+    p.gu_done = counters + chunks;
     p.status = st;
     p.wait_limit_ns = kWaitLimitNs;
     const int total = p.tiles_gu + p.tiles_dn;
     const int pairs = total < max_pairs ? total : max_pairs;
-    if (cudaMemsetAsync(counters, 0, fused_counter_bytes(M, P), s) != cudaSuccess) return SPTP_ERR_CUDA;
+    if (cudaMemsetAsync(counters, 0, fused_counter_bytes(M, P, chunks), s) != cudaSuccess) return SPTP_ERR_CUDA;
     const cudaError_t e = launch_boundary_fused(p, pairs, s);
     if (e == cudaSuccess) return SPTP_OK;
-    // A launch that the runtime rejects (for example a cooperative cluster
-    // launch it does not support) enqueues nothing; use the three-launch path.
     cudaGetLastError();
-    if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidValue || e == cudaErrorNotSupported ||
-        e == cudaErrorInvalidConfiguration) {
-        unavailable[dev & 63] = true;
-        return SPTP_ERR_UNSUPPORTED;
-    }
-    return SPTP_ERR_CUDA;
+    return launch_rejected(e) ? SPTP_ERR_UNIMPLEMENTED : SPTP_ERR_CUDA;
 }
 
 // The bf16 boundary in front of attention as one persistent launch
 // (fused.cu with qkv set: prologue rows feed each shard's column-parallel QKV
-// GEMM).  Returns SPTP_ERR_UNSUPPORTED, having enqueued nothing, where it
-// cannot launch.
+// GEMM).  The caller has checked fused_runs(); returns as fused_forward.
 int fused_attn_forward(const void* x, const void* partials, const void* gamma, const void* Wqkv, int M, int d,
                        int N, int P, int chunks, float eps, void* qkv_out, void* resid_out, void* y, int* counters,
                        DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {
-    static bool unavailable[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (unavailable[dev & 63]) return SPTP_ERR_UNSUPPORTED;
     const int max_pairs = fused_max_pairs(di.sms);
-    if (max_pairs <= 0) {
-        unavailable[dev & 63] = true;
-        return SPTP_ERR_UNSUPPORTED;
-    }
     const size_t es = 2;
     const int n = N / P;
     const size_t act = static_cast<size_t>(M) * d * es;
@@ -276,39 +253,27 @@ int fused_attn_forward(const void* x, const void* partials, const void* gamma, c
     p.tiles_gu = P * p.mt * p.nt_gu;
     p.tiles_dn = 0;
     p.block_rows = P + 1 <= 5 && d <= 4096 ? 1 : 0;
-    p.rb_ready = counters;
-    p.gu_done = counters;  // unused without down tiles
+    p.chunks = chunks;
+    p.chunk_rows = chunk_rows;
+    p.chunk_ready = counters;
+    p.gu_done = nullptr;  // no down tiles
     p.status = st;
     p.wait_limit_ns = kWaitLimitNs;
     const int pairs = p.tiles_gu < max_pairs ? p.tiles_gu : max_pairs;
-    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(p.mt) * sizeof(int), s) != cudaSuccess) return SPTP_ERR_CUDA;
+    if (cudaMemsetAsync(counters, 0, static_cast<size_t>(chunks) * sizeof(int), s) != cudaSuccess)
+        return SPTP_ERR_CUDA;
     const cudaError_t e = launch_boundary_fused(p, pairs, s);
     if (e == cudaSuccess) return SPTP_OK;
     cudaGetLastError();
-    if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidValue || e == cudaErrorNotSupported ||
-        e == cudaErrorInvalidConfiguration) {
-        unavailable[dev & 63] = true;
-        return SPTP_ERR_UNSUPPORTED;
-    }
-    return SPTP_ERR_CUDA;
+    return launch_rejected(e) ? SPTP_ERR_UNIMPLEMENTED : SPTP_ERR_CUDA;
 }
 
 // The whole bf16 Delayed-TP stack as one persistent launch (fused_dtp.cu).
-// Returns SPTP_ERR_UNSUPPORTED, having enqueued nothing, where it cannot run.
+// The caller has checked dtp_fused_runs(); returns as fused_forward.
 int dtp_fused_forward(void* x_shards, const void* gamma, const void* W1g, const void* W1u, const void* W2, int M,
                       int d, int F, int P, int L, int delta, int flush, float eps, void* ybase, void* sbuf,
                       void* ring, int S, int* counters, DeviceStatus* st, const DevInfo& di, cudaStream_t s) {
-    static bool unavailable[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (unavailable[dev & 63]) return SPTP_ERR_UNSUPPORTED;
-    // the kernel numbers prologue rows with 32 bits
-    if (static_cast<long long>(P) * M * (L + 1) >= (1ll << 31)) return SPTP_ERR_UNSUPPORTED;
     const int max_pairs = dtp_fused_max_pairs(di.sms);
-    if (max_pairs <= 0) {
-        unavailable[dev & 63] = true;
-        return SPTP_ERR_UNSUPPORTED;
-    }
     const int f = F / P;
     const uint64_t es = 2;
     DtpFusedParams p;
@@ -378,56 +343,35 @@ int dtp_fused_forward(void* x_shards, const void* gamma, const void* W1g, const 
     const cudaError_t e = launch_dtp_fused(p, pairs, s);
     if (e == cudaSuccess) return SPTP_OK;
     cudaGetLastError();
-    if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidValue || e == cudaErrorNotSupported ||
-        e == cudaErrorInvalidConfiguration) {
-        unavailable[dev & 63] = true;
-        return SPTP_ERR_UNSUPPORTED;
-    }
-    return SPTP_ERR_CUDA;
+    return launch_rejected(e) ? SPTP_ERR_UNIMPLEMENTED : SPTP_ERR_CUDA;
 }
 
 }  // namespace
 
-extern "C" {
+namespace sptp {
 
-const char* sptp_status_string(int status) {
-    switch (status) {
-        case SPTP_OK: return "ok";
-        case SPTP_ERR_NULL: return "a required pointer is NULL";
-        case SPTP_ERR_SHAPE: return "a size or divisibility rule is violated";
-        case SPTP_ERR_DTYPE: return "unknown dtype";
-        case SPTP_ERR_WORKSPACE: return "workspace too small";
-        case SPTP_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
-        case SPTP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
-        case SPTP_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
-        case SPTP_ERR_ALIAS: return "an output overlaps an input";
-        case SPTP_ERR_TOO_LARGE: return "problem needs more scratch than the static no-allocation array holds";
-        default: return "unknown status";
-    }
-}
-
-size_t sptp_ffn_workspace_size(int M, int d, int F, int P, int chunks, int dtype) {
-    if (check_common(M, d, F, P, dtype) != SPTP_OK || chunks < 1) return 0;
-    const size_t es = esize(dtype);
-    return SPTP_WS_HEADER_BYTES + align_up(static_cast<size_t>(M) * d * es) +
-           align_up(static_cast<size_t>(M) * F * es) + align_up(fused_counter_bytes(M, P));
-}
-
-int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, const void* W1g, const void* W1u,
-                     const void* W2, int M, int d, int F, int P, int chunks, float eps, int dtype, void* out,
-                     void* resid_out, void* workspace, size_t ws_bytes, void* cuda_stream) {
+// Every argument check of sptp_ffn_forward_ex, in order, with no CUDA call;
+// also used by the no-allocation entry point before it touches its scratch.
+int check_ffn_forward_args(const void* x, const void* partials, const void* gamma, const void* W1g,
+                           const void* W1u, const void* W2, int M, int d, int F, int P, int chunks, float eps,
+                           int dtype, const void* out, const void* resid_out, const void* workspace,
+                           size_t ws_bytes, int variant) {
     // activations of an empty sequence (M == 0) may be NULL
     if (!gamma || !W1g || !W1u || !W2 || !workspace || (M != 0 && (!x || !partials || !out)))
         return SPTP_ERR_NULL;
-    int rc = check_common(M, d, F, P, dtype);
+    const int rc = check_common(M, d, F, P, dtype);
     if (rc != SPTP_OK) return rc;
     if (chunks < 1 || chunks % P != 0 || (M > 0 && M % chunks != 0)) return SPTP_ERR_SHAPE;
+    // the launch plan: AUTO is PAIR; CHAIN and FUSED are bf16 only
+    const int v = variant == SPTP_VARIANT_AUTO ? SPTP_VARIANT_PAIR : variant;
+    if (!variant_known(variant) || v == SPTP_VARIANT_LAYERS || (dtype != SPTP_BF16 && v != SPTP_VARIANT_PAIR))
+        return SPTP_ERR_UNIMPLEMENTED;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
     const void* ptrs[] = {x, partials, gamma, W1g, W1u, W2, out, resid_out, workspace};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return SPTP_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return SPTP_ERR_SHAPE;
-    const size_t need = sptp_ffn_workspace_size(M, d, F, P, chunks, dtype);
+    const size_t need = sptp_ffn_workspace_size(M, d, F, P, chunks, static_cast<sptp_dtype>(dtype));
     if (ws_bytes < need) return SPTP_ERR_WORKSPACE;
     const size_t es = esize(dtype);
     const size_t act = static_cast<size_t>(M) * d * es;
@@ -448,9 +392,67 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
         for (int i = 0; i < 7; ++i)
             if (overlaps(resid_out, act, rins[i], rsz[i])) return SPTP_ERR_ALIAS;
     }
+    return SPTP_OK;
+}
+
+// SPTP_OK if the current device is the one the kernels are built for.
+int current_device_ok() {
+    DevInfo di;
+    return device_info(&di);
+}
+
+}  // namespace sptp
+
+extern "C" {
+
+const char* sptp_status_string(int status) {
+    switch (status) {
+        case SPTP_OK: return "ok";
+        case SPTP_ERR_NULL: return "a required pointer is NULL";
+        case SPTP_ERR_SHAPE: return "a size or divisibility rule is violated";
+        case SPTP_ERR_DTYPE: return "unknown dtype";
+        case SPTP_ERR_WORKSPACE: return "workspace too small";
+        case SPTP_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+        case SPTP_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+        case SPTP_ERR_UNIMPLEMENTED:
+            return "the requested variant does not exist for this entry point and dtype, or cannot launch here";
+        case SPTP_ERR_ALIAS: return "an output overlaps an input";
+        case SPTP_ERR_TOO_LARGE: return "problem needs more scratch than the static no-allocation array holds";
+        case SPTP_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
+        case SPTP_ERR_BOUNDS: return "a bounds check of the checked build failed (the access was skipped)";
+        default: return "unknown status";
+    }
+}
+
+size_t sptp_ffn_workspace_size(int M, int d, int F, int P, int chunks, sptp_dtype dtype) {
+    if (check_common(M, d, F, P, dtype) != SPTP_OK || chunks < 1) return 0;
+    const size_t es = esize(dtype);
+    return SPTP_WS_HEADER_BYTES + align_up(static_cast<size_t>(M) * d * es) +
+           align_up(static_cast<size_t>(M) * F * es) + align_up(fused_counter_bytes(M, P, chunks));
+}
+
+int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, const void* W1g, const void* W1u,
+                     const void* W2, int M, int d, int F, int P, int chunks, float eps, sptp_dtype dtype, void* out,
+                     void* resid_out, void* workspace, size_t ws_bytes, void* cuda_stream) {
+    return sptp_ffn_forward_ex(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, dtype, out, resid_out,
+                               workspace, ws_bytes, cuda_stream, SPTP_VARIANT_AUTO);
+}
+
+int sptp_ffn_forward_ex(const void* x, const void* partials, const void* gamma, const void* W1g, const void* W1u,
+                        const void* W2, int M, int d, int F, int P, int chunks, float eps, sptp_dtype dtype,
+                        void* out, void* resid_out, void* workspace, size_t ws_bytes, void* cuda_stream,
+                        sptp_variant variant) {
+    int rc = check_ffn_forward_args(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, dtype, out,
+                                    resid_out, workspace, ws_bytes, variant);
+    if (rc != SPTP_OK) return rc;
+    const int v = variant == SPTP_VARIANT_AUTO ? SPTP_VARIANT_PAIR : variant;
+    const size_t es = esize(dtype);
+    const size_t act = static_cast<size_t>(M) * d * es;
     if (M == 0) return SPTP_OK;
     DevInfo di;
     if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    if ((v == SPTP_VARIANT_FUSED || v == SPTP_VARIANT_CHAIN) && !fused_runs(di, M, chunks))
+        return SPTP_ERR_UNIMPLEMENTED;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
 
@@ -460,12 +462,9 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
         mptr(workspace, SPTP_WS_HEADER_BYTES + align_up(act) + align_up(static_cast<size_t>(M) * F * es)));
     const int band = raster_band();
 
-    if (dtype == SPTP_BF16 && gemm_variant() == Variant::kFused) {
-        rc = fused_forward(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, out, resid_out, y, sbuf,
-                           counters, ws_status(workspace), band, di, s);
-        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
-        if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: the three-launch path below
-    }
+    if (v == SPTP_VARIANT_FUSED)
+        return fused_forward(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, out, resid_out, y, sbuf,
+                             counters, ws_status(workspace), band, di, s);
 
     // 1-3: reduce-scatter arithmetic, residual add, RMSNorm (every chunk)
     PrologueParams pp;
@@ -481,12 +480,12 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
     pp.wait_limit_ns = kWaitLimitNs;
     if ((rc = cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, s))) != SPTP_OK) return rc;
 
-    if (dtype == SPTP_BF16 && gemm_variant() == Variant::kChain) {
+    if (v == SPTP_VARIANT_CHAIN) {
         // 4-7 as one persistent launch: gate/up and down tiles in one sequence
+        // (the prologue above has run: a refused launch is a launch failure)
         rc = fused_forward(x, partials, gamma, W1g, W1u, W2, M, d, F, P, chunks, eps, out, resid_out, y, sbuf,
                            counters, ws_status(workspace), band, di, s, true);
-        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
-        if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: the two GEMM launches below
+        return rc == SPTP_ERR_UNIMPLEMENTED ? SPTP_ERR_CUDA : rc;
     }
 
     // 4-6: chunked gather (identity) + column-parallel gate/up + SwiGLU,
@@ -502,7 +501,7 @@ int sptp_ffn_forward(const void* x, const void* partials, const void* gamma, con
     return down(sbuf, W2, M, d, F, P, dtype, outs, ws_status(workspace), band, di, s);
 }
 
-size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta, int dtype) {
+size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta, sptp_dtype dtype) {
     if (check_common(M, d, F, P, dtype) != SPTP_OK || L < 1 || delta < 0) return 0;
     const size_t es = esize(dtype);
     const size_t S = static_cast<size_t>(delta + 1 < L ? delta + 1 : L);
@@ -512,11 +511,22 @@ size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta
 }
 
 int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, const void* W1u, const void* W2,
-                          int M, int d, int F, int P, int L, int delta, int flush, float eps, int dtype,
+                          int M, int d, int F, int P, int L, int delta, int flush, float eps, sptp_dtype dtype,
                           void* workspace, size_t ws_bytes, void* cuda_stream) {
+    return dtp_ffn_stack_forward_ex(x_shards, gamma, W1g, W1u, W2, M, d, F, P, L, delta, flush, eps, dtype,
+                                    workspace, ws_bytes, cuda_stream, SPTP_VARIANT_AUTO);
+}
+
+int dtp_ffn_stack_forward_ex(void* x_shards, const void* gamma, const void* W1g, const void* W1u, const void* W2,
+                             int M, int d, int F, int P, int L, int delta, int flush, float eps, sptp_dtype dtype,
+                             void* workspace, size_t ws_bytes, void* cuda_stream, sptp_variant variant) {
     if (!gamma || !W1g || !W1u || !W2 || !workspace || (M != 0 && !x_shards)) return SPTP_ERR_NULL;
     int rc = check_common(M, d, F, P, dtype);
     if (rc != SPTP_OK) return rc;
+    // AUTO: the fused stack for bf16 where it can run, else per-module launches
+    if (!variant_known(variant) || variant == SPTP_VARIANT_PAIR || variant == SPTP_VARIANT_CHAIN ||
+        (dtype != SPTP_BF16 && variant == SPTP_VARIANT_FUSED))
+        return SPTP_ERR_UNIMPLEMENTED;
     if (L < 1 || delta < 0) return SPTP_ERR_SHAPE;
     const int S = delta + 1 < L ? delta + 1 : L;
     if (1 + (P - 1) * S > kMaxSrcPerGroup) return SPTP_ERR_SHAPE;
@@ -537,6 +547,8 @@ int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, co
     if (M == 0) return SPTP_OK;
     DevInfo di;
     if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    const bool fused_ok = dtype == SPTP_BF16 && dtp_fused_runs(di, M, P, L);
+    if (variant == SPTP_VARIANT_FUSED && !fused_ok) return SPTP_ERR_UNIMPLEMENTED;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
 
@@ -545,11 +557,12 @@ int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, co
     char* sbuf = ybase + align_up(act * P);
     char* ring = sbuf + align_up(static_cast<size_t>(M) * F * es);
     int* counters = reinterpret_cast<int*>(ring + align_up(static_cast<size_t>(S) * P * act));
-    if (dtype == SPTP_BF16 && dtp_fused_selected()) {
+    if (fused_ok && variant != SPTP_VARIANT_LAYERS) {
         rc = dtp_fused_forward(x_shards, gamma, W1g, W1u, W2, M, d, F, P, L, delta, flush, eps, ybase, sbuf, ring, S,
                                counters, ws_status(workspace), di, s);
-        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
-        if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: launches per module below
+        // a launch the runtime refused enqueued nothing: AUTO takes the
+        // per-module launches below
+        if (rc != SPTP_ERR_UNIMPLEMENTED || variant == SPTP_VARIANT_FUSED) return rc;
     }
     auto xs = [&](int p) { return mptr(x_shards, static_cast<size_t>(p) * act); };
     auto yp = [&](int p) { return ybase + static_cast<size_t>(p) * act; };
@@ -602,7 +615,7 @@ int dtp_ffn_stack_forward(void* x_shards, const void* gamma, const void* W1g, co
 }
 
 int sptp_prologue(const void* x, const void* partials, const void* gamma, int M, int d, int P, float eps,
-                  int dtype, void* h_out, void* y_out, void* cuda_stream) {
+                  sptp_dtype dtype, void* h_out, void* y_out, void* cuda_stream) {
     if (!gamma || (M != 0 && (!x || !partials || !y_out))) return SPTP_ERR_NULL;
     int rc = check_common(M, d, 8 * P, P, dtype);
     if (rc != SPTP_OK) return rc;
@@ -635,7 +648,7 @@ int sptp_prologue(const void* x, const void* partials, const void* gamma, int M,
     return cuda_status(launch_prologue(pp, dtype == SPTP_BF16, di.sms, static_cast<cudaStream_t>(cuda_stream)));
 }
 
-int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u, int M, int d, int F, int P, int dtype,
+int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u, int M, int d, int F, int P, sptp_dtype dtype,
                        void* s_out, void* workspace, size_t ws_bytes, void* cuda_stream) {
     if (!W1g || !W1u || !workspace || (M != 0 && (!y || !s_out))) return SPTP_ERR_NULL;
     int rc = check_common(M, d, F, P, dtype);
@@ -659,7 +672,7 @@ int sptp_gateup_swiglu(const void* y, const void* W1g, const void* W1u, int M, i
     return gateup(A, W1g, W1u, M, d, F, P, dtype, s_out, ws_status(workspace), raster_band(), di, s);
 }
 
-int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype, void* out,
+int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P, sptp_dtype dtype, void* out,
                    void* workspace, size_t ws_bytes, void* cuda_stream) {
     if (!W2 || !workspace || (M != 0 && (!s_in || !out))) return SPTP_ERR_NULL;
     int rc = check_common(M, d, F, P, dtype);
@@ -684,19 +697,33 @@ int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P,
     return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), raster_band(), di, s);
 }
 
-size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, int dtype) {
+size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, sptp_dtype dtype) {
     if (check_common(M, d, N, P, dtype) != SPTP_OK || chunks < 1) return 0;
     return SPTP_WS_HEADER_BYTES + align_up(static_cast<size_t>(M) * d * esize(dtype)) +
-           align_up(static_cast<size_t>((M + 255) / 256) * sizeof(int));
+           align_up(static_cast<size_t>(chunks) * sizeof(int));
 }
 
 int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma, const void* Wqkv, int M, int d,
-                          int N, int P, int chunks, float eps, int dtype, void* qkv_out, void* resid_out,
+                          int N, int P, int chunks, float eps, sptp_dtype dtype, void* qkv_out, void* resid_out,
                           void* workspace, size_t ws_bytes, void* cuda_stream) {
+    return sptp_attn_qkv_forward_ex(x, partials, gamma, Wqkv, M, d, N, P, chunks, eps, dtype, qkv_out, resid_out,
+                                    workspace, ws_bytes, cuda_stream, SPTP_VARIANT_AUTO);
+}
+
+int sptp_attn_qkv_forward_ex(const void* x, const void* partials, const void* gamma, const void* Wqkv, int M,
+                             int d, int N, int P, int chunks, float eps, sptp_dtype dtype, void* qkv_out,
+                             void* resid_out, void* workspace, size_t ws_bytes, void* cuda_stream,
+                             sptp_variant variant) {
     if (!gamma || !Wqkv || !workspace || (M != 0 && (!x || !partials || !qkv_out))) return SPTP_ERR_NULL;
     int rc = check_common(M, d, N, P, dtype);
     if (rc != SPTP_OK) return rc;
     if (chunks < 1 || chunks % P != 0 || (M > 0 && M % chunks != 0)) return SPTP_ERR_SHAPE;
+    // the launch plan: AUTO is PAIR (prologue + one column-parallel GEMM);
+    // FUSED is bf16 only; there is no CHAIN or LAYERS form
+    const int v = variant == SPTP_VARIANT_AUTO ? SPTP_VARIANT_PAIR : variant;
+    if (!variant_known(variant) || (v != SPTP_VARIANT_PAIR && v != SPTP_VARIANT_FUSED) ||
+        (dtype != SPTP_BF16 && v == SPTP_VARIANT_FUSED))
+        return SPTP_ERR_UNIMPLEMENTED;
     if (!(eps >= 0.f) || !std::isfinite(eps)) return SPTP_ERR_SHAPE;
     const void* ptrs[] = {x, partials, gamma, Wqkv, qkv_out, resid_out, workspace};
     for (const void* q : ptrs)
@@ -724,16 +751,14 @@ int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma
     if (M == 0) return SPTP_OK;
     DevInfo di;
     if ((rc = device_info(&di)) != SPTP_OK) return rc;
+    if (v == SPTP_VARIANT_FUSED && !fused_runs(di, M, chunks)) return SPTP_ERR_UNIMPLEMENTED;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     void* y = mptr(workspace, SPTP_WS_HEADER_BYTES);
     int* counters = reinterpret_cast<int*>(mptr(workspace, SPTP_WS_HEADER_BYTES + align_up(act)));
-    if (dtype == SPTP_BF16 && attn_fused_selected()) {
-        rc = fused_attn_forward(x, partials, gamma, Wqkv, M, d, N, P, chunks, eps, qkv_out, resid_out, y, counters,
-                                ws_status(workspace), raster_band(), di, s);
-        if (rc == SPTP_ERR_UNSUPPORTED && strict_variant()) return SPTP_ERR_CUDA;
-        if (rc != SPTP_ERR_UNSUPPORTED) return rc;  // else: prologue + GEMM below
-    }
+    if (v == SPTP_VARIANT_FUSED)
+        return fused_attn_forward(x, partials, gamma, Wqkv, M, d, N, P, chunks, eps, qkv_out, resid_out, y,
+                                  counters, ws_status(workspace), raster_band(), di, s);
     PrologueParams pp;
     std::memset(&pp, 0, sizeof(pp));
     pp.G = 1;
@@ -751,7 +776,7 @@ int sptp_attn_qkv_forward(const void* x, const void* partials, const void* gamma
 }
 
 int sptp_permute_ffn_neurons(const void* W1g, const void* W1u, const void* W2, const int* perm, int L, int d,
-                             int F, int dtype, void* W1g_out, void* W1u_out, void* W2_out, void* workspace,
+                             int F, sptp_dtype dtype, void* W1g_out, void* W1u_out, void* W2_out, void* workspace,
                              size_t ws_bytes, void* cuda_stream) {
     if (!W1g || !W1u || !W2 || !perm || !W1g_out || !W1u_out || !W2_out || !workspace) return SPTP_ERR_NULL;
     int rc = check_common(8, d, F, 1, dtype);

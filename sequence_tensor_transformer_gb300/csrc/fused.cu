@@ -5,15 +5,14 @@
 //
 // One launch of CTA pairs (cta_group::2, one CTA per SM, all co-resident)
 // computes the whole boundary:
-//   warps 6..13  prologue: rows r = w, w + W, ... (W prologue warps in the
-//                grid) in sequence order: h = x + sum_p partials[p], y =
-//                RMSNorm(h) * gamma; after each row a release increment of
-//                the row's 256-row block counter (rows become "gathered" as
-//                soon as they are produced)
+//   warps 6..13  prologue: rows in sequence order: h = x + sum_p
+//                partials[p], y = RMSNorm(h) * gamma; after each row a
+//                release increment of its sequence chunk's counter (a chunk
+//                is "gathered" once all its rows are produced)
 //   warp 0       TMA producer: before a gate/up tile's first A load it waits
-//                (bounded) until the tile's 256 rows of y are ready; before a
-//                down tile's, until every gate/up tile of its (shard, rows)
-//                has been stored
+//                (bounded) until every sequence chunk its 256 rows overlap is
+//                complete; before a down tile's, until every gate/up tile of
+//                its (shard, rows) has been stored
 //   warp 1       MMA issuer of the even CTA (M=256, N=256, K=16 UMMAs)
 //   warps 2..5   epilogue: SwiGLU into s (then a release increment of the
 //                (shard, 256-row block) counter) or the bf16 partials out
@@ -269,7 +268,7 @@ __device__ __forceinline__ void prologue_block_rows(const FusedParams& p, int ti
         // make this warp's part of y visible to the TMA loads of other CTAs
         fence_proxy_async_global();
         __syncwarp();
-        if (lane == 0) red_release_add(&p.rb_ready[row >> 8], 1);
+        if (lane == 0) red_release_add(&p.chunk_ready[row / p.chunk_rows], 1);
     }
 }
 
@@ -370,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             // make the row's y visible to the TMA loads of other CTAs
             fence_proxy_async_global();
             __syncwarp();
-            if (lane == 0) red_release_add(&p.rb_ready[row >> 8], 1);
+            if (lane == 0) red_release_add(&p.chunk_ready[row / p.chunk_rows], 1);
         }
     } else if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -385,9 +384,12 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             // dependency of this tile's A operand
             if (!tl.down) {
                 if (!p.pre_normed) {
-                    // a row counts once per publishing warp
-                    const int need = min(PBM, p.M - tl.m * PBM) * (p.block_rows ? PRO_WARPS : 1);
-                    ok = flag_wait_geq(&p.rb_ready[tl.m], need, wc, kWhereFusedRows, t);
+                    // every chunk the tile's rows overlap; a row counts once
+                    // per publishing warp
+                    const int need = p.chunk_rows * (p.block_rows ? PRO_WARPS : 1);
+                    const int c1 = (min(p.M, (tl.m + 1) * PBM) - 1) / p.chunk_rows;
+                    for (int c = tl.m * PBM / p.chunk_rows; ok && c <= c1; ++c)
+                        ok = flag_wait_geq(&p.chunk_ready[c], need, wc, kWhereFusedRows, t);
                 }
             } else {
                 ok = flag_wait_geq(&p.gu_done[tl.g * p.mt + tl.m], 2 * p.nt_gu, wc, kWhereFusedGateUp, t);

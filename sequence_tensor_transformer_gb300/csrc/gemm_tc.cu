@@ -1,22 +1,21 @@
-// Persistent tcgen05 GEMM for sm_103a with TMA-fed shared-memory pipeline and
-// TMEM accumulators, used for the column-parallel gate/up projection (with a
-// fused SwiGLU epilogue) and the row-parallel down projection (with a bf16
-// partial-store epilogue) of the SP-TP FFN boundary ("[Feature] Async Tensor
-// Parallelism for Archon Engine", "Potential Solution").
+// Persistent tcgen05 GEMM for sm_103a on CTA pairs (cta_group::2), with a
+// TMA-fed shared-memory pipeline and TMEM accumulators, used for the
+// column-parallel gate/up projection (with a fused SwiGLU epilogue) and the
+// row-parallel down projection (with a bf16 partial-store epilogue) of the
+// SP-TP FFN boundary ("[Feature] Async Tensor Parallelism for Archon Engine",
+// "Potential Solution").
 //
-// One CTA per SM, 6 warps:
-//   warp 0      TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage
-//   warp 1      MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16) per stage into
-//               one of two TMEM accumulators of 256 fp32 columns
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, SwiGLU or bf16
-//               convert, 16-byte global stores; overlaps the next tile's MMAs
-// Tiles are walked in raster bands of `band` m-tiles (4096 rows) so
-// that concurrently running CTAs share A and B tiles in L2.
-//
-// The CTA-pair kernel (namespace pair, cta_group::2) is the default: tiles of
-// 256 rows x 256 B rows, each CTA of a cluster pair staging its own 128 rows
-// of A and of B, one MMA thread on the even CTA, six 32 KiB stages.  It runs
-// on bf16 operands (kind::f16, 64 elements per 128-byte row) or on E4M3
+// A cluster of two CTAs, one per SM, computes 256 x 256 tiles; each CTA
+// stages its own 128 rows of A and of B in six 32 KiB stages:
+//   warp 0      TMA producer (both CTAs)
+//   warp 1      MMA issuer of the even CTA: 4 x tcgen05.mma (M=256, N=256,
+//               K=16) per stage into one of two TMEM accumulators of 256
+//               fp32 columns
+//   warps 2..5  epilogue (both CTAs): tcgen05.ld of the accumulator, SwiGLU
+//               or bf16 convert, global stores; overlaps the next tile's MMAs
+// Tiles are walked in raster bands of `band` m-tiles (4096 rows) so that
+// concurrently running pairs share A and B tiles in L2.  The kernel runs on
+// bf16 operands (kind::f16, 64 elements per 128-byte row) or on E4M3
 // operands (kind::f8f6f4, 128 per row) for the fp8 linear layers ("[Feature]
 // Async Tensor Parallelism for Archon Engine", "Additional Information"),
 // whose epilogue multiplies the fp32 accumulator by the token row's and the
@@ -33,29 +32,9 @@ namespace sptp {
 
 namespace {
 
-constexpr int BM = 128;              // rows of A per tile (TMEM lanes)
-constexpr int BN = 256;              // B rows per tile (UMMA N)
-constexpr int BK = 64;               // K elements per stage (one 128-byte swizzle row)
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int TMEM_COLS = 512;       // two accumulators of BN fp32 columns
-constexpr int NUM_THREADS = 192;
+constexpr int BK = 64;               // K elements per stage (one 128-byte swizzle row of bf16)
+constexpr int TMEM_COLS = 512;       // two accumulators of 256 fp32 columns
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + BAR_BYTES;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-
-struct SmemBarriers {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
-    uint64_t drain;
-    uint32_t tmem_base;
-    int abort_flag;
-};
-static_assert(sizeof(SmemBarriers) <= BAR_BYTES, "barrier block too large");
 
 __device__ __forceinline__ void decode_tile(const TcGemmParams& p, int t, int& g, int& m, int& n) {
     const int per_band = p.band * p.G * p.nt;
@@ -79,205 +58,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <Epi EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcGemmParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    uint8_t* a_tiles = smem;
-    uint8_t* b_tiles = smem + STAGES * A_STAGE_BYTES;
-    SmemBarriers* bars = reinterpret_cast<SmemBarriers*>(smem + STAGES * STAGE_BYTES);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&bars->acc_full[a], 1);
-            mbar_init(&bars->acc_empty[a], 4 * 32);
-        }
-        mbar_init(&bars->drain, 1);
-        bars->abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        for (int g = 0; g < p.G; ++g) {
-            tma_prefetch_map(&p.mapA[g]);
-            tma_prefetch_map(&p.mapB0[g]);
-            if (EPI == Epi::kSwiGLU) tma_prefetch_map(&p.mapB1[g]);
-        }
-    }
-    if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = bars->tmem_base;
-
-    WaitCtx wc{p.status, &bars->abort_flag, p.wait_limit_ns};
-    const int total = p.G * p.mt * p.nt;
-
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ TMA producer
-        int stage = 0;
-        uint32_t phase = 0;
-        int armed_parity[STAGES];
-        for (int s = 0; s < STAGES; ++s) armed_parity[s] = -1;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            int g, m, n;
-            decode_tile(p, t, g, m, n);
-            for (int kb = 0; kb < p.nk; ++kb) {
-                if (!mbar_wait(&bars->empty[stage], phase ^ 1u, wc, kWhereProducerEmpty, t)) {
-                    ok = false;
-                    break;
-                }
-                uint64_t* fb = &bars->full[stage];
-                mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                armed_parity[stage] = static_cast<int>(phase);
-                tma_load_2d(a_tiles + stage * A_STAGE_BYTES, &p.mapA[g], fb, kb * BK, m * BM);
-                uint8_t* bt = b_tiles + stage * B_STAGE_BYTES;
-                if (EPI == Epi::kSwiGLU) {
-                    tma_load_2d(bt, &p.mapB0[g], fb, kb * BK, n * (BN / 2));
-                    tma_load_2d(bt + B_STAGE_BYTES / 2, &p.mapB1[g], fb, kb * BK, n * (BN / 2));
-                } else {
-                    tma_load_2d(bt, &p.mapB0[g], fb, kb * BK, n * BN);
-                }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-        // Every copy this thread started must have landed before the CTA
-        // exits (normally they have; after an abort, wait a bounded time).
-        WaitCtx drain{p.status, &bars->abort_flag, p.wait_limit_ns};
-        int dummy_abort = 0;
-        drain.abort_flag = &dummy_abort;
-        for (int s = 0; s < STAGES; ++s)
-            if (armed_parity[s] >= 0)
-                mbar_wait(&bars->full[s], static_cast<uint32_t>(armed_parity[s]), drain, kWhereDrain, s);
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        int local = 0;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++local) {
-            const int acc = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
-            if (!mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, wc, kWhereMmaAccEmpty, t)) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-            for (int kb = 0; kb < p.nk; ++kb) {
-                if (!mbar_wait(&bars->full[stage], phase, wc, kWhereMmaFull, t)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(a_tiles + stage * A_STAGE_BYTES));
-                const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(b_tiles + stage * B_STAGE_BYTES));
-#pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    // advance 16 elements (32 bytes) along K inside the swizzle row
-                    umma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, IDESC, (kb | k) != 0 ? 1u : 0u);
-                }
-                umma_commit(&bars->empty[stage]);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (!ok) break;
-            umma_commit(&bars->acc_full[acc]);
-        }
-        // all MMAs issued by this thread complete before TMEM is released
-        umma_commit(&bars->drain);
-        WaitCtx drain{p.status, &bars->abort_flag, p.wait_limit_ns};
-        int dummy_abort = 0;
-        drain.abort_flag = &dummy_abort;
-        mbar_wait(&bars->drain, 0, drain, kWhereDrain, -1);
-    } else if (warp >= 2) {
-        // ------------------------------------------------ epilogue
-        const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter+32)
-        const int row_in_tile = quarter * 32 + lane;
-        int local = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x, ++local) {
-            const int acc = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
-            const bool ok = mbar_wait(&bars->acc_full[acc], acc_phase, wc, kWhereEpilogueAccFull, t);
-            // tcgen05.ld is warp-collective: leave together if any lane gave up
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            int g, m, n;
-            decode_tile(p, t, g, m, n);
-            const int row = m * BM + row_in_tile;
-            const bool row_ok = row < p.M;
-            const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out[g]) + static_cast<long long>(row) * p.ldo;
-            if (EPI == Epi::kSwiGLU) {
-#pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 32) {
-                    uint32_t gv[32], uv[32];
-                    tmem_ld_32cols(taddr + c, gv);
-                    tmem_ld_32cols(taddr + BN / 2 + c, uv);
-                    tmem_ld_wait();
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float a0 = __uint_as_float(gv[2 * j]), a1 = __uint_as_float(gv[2 * j + 1]);
-                        const float b0 = __uint_as_float(uv[2 * j]), b1 = __uint_as_float(uv[2 * j + 1]);
-                        packed[j] = pack_bf16x2(silu_f(a0) * b0, silu_f(a1) * b1);
-                    }
-                    const int col = n * (BN / 2) + c;
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            if (col + 8 * v < p.N)
-                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
-                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t v32[32];
-                    tmem_ld_32cols(taddr + c, v32);
-                    tmem_ld_wait();
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        packed[j] = pack_bf16x2(__uint_as_float(v32[2 * j]), __uint_as_float(v32[2 * j + 1]));
-                    const int col = n * BN + c;
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            if (col + 8 * v < p.N)
-                                *reinterpret_cast<uint4*>(out + col + 8 * v) =
-                                    make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-                    }
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&bars->acc_empty[acc]);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
-}
-
 // ---------------------------------------------------------------------------
-// CTA-pair variant (cta_group::2, cluster of 2): the pair computes a
+// The CTA-pair kernel (cta_group::2, cluster of 2): the pair computes a
 // 256 x 256 tile.  Each CTA stages its own 128 A rows and one half of the B
 // tile (SwiGLU: CTA 0 the 128 gate rows, CTA 1 the 128 up rows; plain: the
 // two 128-row halves), so a stage is 32 KiB per CTA and 6 stages fit.  The
@@ -618,8 +400,6 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 }  // namespace
 
-size_t tc_gemm_smem_bytes() { return SMEM_BYTES; }
-
 bool encode_map_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = get_encode_fn();
@@ -664,25 +444,6 @@ bool encode_map_bf16_nd(CUtensorMap* map, const void* base, int rank, const uint
                     gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s) {
-    const int total = p.G * p.mt * p.nt;
-    if (total == 0) return cudaSuccess;
-    const int grid = total < num_sms ? total : num_sms;
-    cudaError_t e;
-    if (epi == Epi::kSwiGLU) {
-        e = cudaFuncSetAttribute(tc_gemm_kernel<Epi::kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        tc_gemm_kernel<Epi::kSwiGLU><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    } else {
-        e = cudaFuncSetAttribute(tc_gemm_kernel<Epi::kStore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        tc_gemm_kernel<Epi::kStore><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    }
-    return cudaGetLastError();
 }
 
 namespace {

@@ -1,36 +1,12 @@
 // GEMM launches shared by the C-ABI entry points: the tensor maps, tile
 // counts and raster band of each grouped GEMM (gate/up + SwiGLU, down,
-// column-parallel store, and their E4M3 forms), and the bf16 execution
-// variant.  The kernels are in gemm_tc.cu (tcgen05) and gemm_simt.cu (fp32).
-#include <cstdlib>
+// column-parallel store, and their E4M3 forms).  The kernels are in
+// gemm_tc.cu (tcgen05 CTA pairs, bf16 and E4M3) and gemm_simt.cu (fp32).
 #include <cstring>
 
 #include "launch.h"
 
 namespace sptp {
-
-// bf16 execution variant, from the environment variable SPTP_GEMM_VARIANT:
-//   unset / "pair"   prologue + CTA-pair gate/up + CTA-pair down launches
-//   "fused"          the whole boundary in one persistent CTA-pair launch
-//                    (falls back to "pair" where it cannot be launched)
-//   "chain"          prologue launch + one persistent CTA-pair launch running
-//                    the gate/up tiles and then the down tiles (falls back to
-//                    "pair" where it cannot be launched)
-//   "single"         prologue + single-CTA gate/up + down launches
-// The step-level entry points use "pair" unless "single" is selected.  On the
-// 8192 x 4096 x 14336 boundary the fused launch and "pair" measure level
-// (1670-1675 vs 1668-1669 TFLOP/s); the fused one needs ~7% fewer SM cycles
-// but, under the GPU's power cap, runs at a lower clock.  "pair" stays the
-// default: its kernels can be profiled with ncu, the cooperative launch not.
-Variant gemm_variant() {
-    const char* v = std::getenv("SPTP_GEMM_VARIANT");
-    if (v != nullptr && std::strcmp(v, "single") == 0) return Variant::kSingle;
-    if (v != nullptr && std::strcmp(v, "fused") == 0) return Variant::kFused;
-    if (v != nullptr && std::strcmp(v, "chain") == 0) return Variant::kChain;
-    return Variant::kPair;
-}
-
-bool use_pair_gemm() { return gemm_variant() != Variant::kSingle; }
 
 // Raster band: the GEMMs walk the m-tiles of 4096 rows against each B panel
 // before moving to the next panel, so the band's A tiles stay in L2 while the
@@ -63,22 +39,19 @@ int gateup(const void* const* A, const void* W1g, const void* W1u, int M, int d,
                 return SPTP_ERR_CUDA;
             p.out[g] = mptr(s_out, static_cast<size_t>(g) * M * f * es);
         }
-        const bool pair = use_pair_gemm();
-        const int bm = pair ? 2 * kBM : kBM;
         p.ldo = f;
         p.M = M;
         p.N = f;
         p.K = d;
         p.G = P;
-        p.mt = (M + bm - 1) / bm;
+        p.mt = (M + 2 * kBM - 1) / (2 * kBM);
         p.nt = (f + kBNSwiGLU - 1) / kBNSwiGLU;
         p.nk = (d + kBK - 1) / kBK;
-        if (pair) band = (band + 1) / 2;
+        band = (band + 1) / 2;
         p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
         p.status = st;
         p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kSwiGLU, di.sms, s)
-                                : launch_tc_gemm(p, Epi::kSwiGLU, di.sms, s));
+        return cuda_status(launch_tc_gemm_pair(p, Epi::kSwiGLU, di.sms, s));
     }
     SimtGemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -106,10 +79,8 @@ int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype
     const size_t es = esize(dtype);
     if (M == 0) return SPTP_OK;
     if (dtype == SPTP_BF16) {
-        const bool pair = use_pair_gemm();
-        const int bm = pair ? 2 * kBM : kBM;
         // a CTA pair stages each B tile as two 128-row halves
-        const uint32_t bbox = pair ? kBNStore / 2 : kBNStore;
+        const uint32_t bbox = kBNStore / 2;
         TcGemmParams p;
         std::memset(&p, 0, sizeof(p));
         for (int g = 0; g < P; ++g) {
@@ -125,15 +96,14 @@ int down(const void* s_in, const void* W2, int M, int d, int F, int P, int dtype
         p.N = d;
         p.K = f;
         p.G = P;
-        p.mt = (M + bm - 1) / bm;
+        p.mt = (M + 2 * kBM - 1) / (2 * kBM);
         p.nt = (d + kBNStore - 1) / kBNStore;
         p.nk = (f + kBK - 1) / kBK;
-        if (pair) band = (band + 1) / 2;
+        band = (band + 1) / 2;
         p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
         p.status = st;
         p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kStore, di.sms, s)
-                                : launch_tc_gemm(p, Epi::kStore, di.sms, s));
+        return cuda_status(launch_tc_gemm_pair(p, Epi::kStore, di.sms, s));
     }
     SimtGemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -161,12 +131,11 @@ int colpar_store(const void* A, const void* W, int M, int K, int N, int P, int d
     const size_t es = esize(dtype);
     if (M == 0) return SPTP_OK;
     if (dtype == SPTP_BF16) {
-        const bool pair = use_pair_gemm();
-        const int bm = pair ? 2 * kBM : kBM;
-        const uint32_t bbox = pair ? kBNStore / 2 : kBNStore;
+        const int bm = 2 * kBM;
+        const uint32_t bbox = kBNStore / 2;
         TcGemmParams p;
         std::memset(&p, 0, sizeof(p));
-        if (pair && P > 1 && n % kBNStore != 0) {
+        if (P > 1 && n % kBNStore != 0) {
             // Every shard reads the same A, so the P shards run as one GEMM
             // over all N rows of W, each 8-column vector stored to its
             // shard's [M][N/P] block: no half-empty last tile per shard
@@ -206,12 +175,11 @@ int colpar_store(const void* A, const void* W, int M, int K, int N, int P, int d
         p.mt = (M + bm - 1) / bm;
         p.nt = (n + kBNStore - 1) / kBNStore;
         p.nk = (K + kBK - 1) / kBK;
-        if (pair) band = (band + 1) / 2;
+        band = (band + 1) / 2;
         p.band = band < 1 ? 1 : (band > p.mt ? p.mt : band);
         p.status = st;
         p.wait_limit_ns = kWaitLimitNs;
-        return cuda_status(pair ? launch_tc_gemm_pair(p, Epi::kStore, di.sms, s)
-                                : launch_tc_gemm(p, Epi::kStore, di.sms, s));
+        return cuda_status(launch_tc_gemm_pair(p, Epi::kStore, di.sms, s));
     }
     SimtGemmParams p;
     std::memset(&p, 0, sizeof(p));

@@ -1,6 +1,6 @@
 // GEMM launch helpers shared by the C-ABI entry points (launch.cu): tile
-// shapes, the raster band, the bf16 execution variant, and the grouped GEMM
-// launches of the boundary.  Sizes are validated by the callers.
+// shapes, the raster band and the grouped GEMM launches of the boundary.
+// Sizes are validated by the callers.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -25,10 +25,6 @@ inline size_t esize(int dtype) { return dtype == SPTP_BF16 ? 2 : 4; }
 inline const char* cptr(const void* base, size_t off_bytes) { return static_cast<const char*>(base) + off_bytes; }
 inline char* mptr(void* base, size_t off_bytes) { return static_cast<char*>(base) + off_bytes; }
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA; }
-
-enum class Variant { kFused, kChain, kPair, kSingle };
-Variant gemm_variant();
-bool use_pair_gemm();
 
 // m-tiles (128 rows) per raster band
 int raster_band();

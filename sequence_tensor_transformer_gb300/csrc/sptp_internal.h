@@ -100,14 +100,12 @@ struct TcGemmParams {
 
 enum class Epi { kSwiGLU, kStore };
 
-cudaError_t launch_tc_gemm(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
-// CTA-pair (cta_group::2) variant: tiles of 256 rows (mt counts 256-row tiles)
-// and 256 B rows; same parameter block and tensor maps (boxes of 128 rows).
+// CTA-pair (cta_group::2) GEMM: tiles of 256 rows (mt counts 256-row tiles)
+// and 256 B rows; tensor maps with boxes of 64 x 128.
 cudaError_t launch_tc_gemm_pair(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
 // The same CTA-pair GEMM on E4M3 operands (tcgen05 kind::f8f6f4; tensor maps
 // of bytes with boxes of 128 x 128), dequantised in the epilogue.
 cudaError_t launch_tc_gemm_pair_e4m3(const TcGemmParams& p, Epi epi, int num_sms, cudaStream_t s);
-size_t tc_gemm_smem_bytes();
 
 // Encodes a 2-D byte (E4M3) tensor map with 128-byte swizzle.
 bool encode_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
@@ -150,12 +148,16 @@ struct FusedParams {
     int qkv;
     // block_rows != 0: the CTA's prologue warps take one row together (needs
     // P + 1 <= 5 sources and d <= 4096); each of them publishes its part, so a
-    // row adds PRO_WARPS to rb_ready
+    // row adds PRO_WARPS to its chunk's counter
     int block_rows;
     // pre_normed != 0: y was written by a preceding prologue launch (stream
     // order); the prologue warps idle and gate/up tiles do not wait for rows
     int pre_normed;
-    int* rb_ready;                     // [mt] prologue rows done per 256-row block
+    // The sequence chunks of the (identity) all-gather: chunk c is rows
+    // [c * chunk_rows, (c + 1) * chunk_rows); a gate/up tile reads its rows of
+    // y once every chunk they overlap is complete.
+    int chunks, chunk_rows;
+    int* chunk_ready;                  // [chunks] prologue rows published per chunk
     int* gu_done;                      // [P][mt] gate/up tile halves stored
     DeviceStatus* status;
     unsigned long long wait_limit_ns;
@@ -212,6 +214,15 @@ cudaError_t launch_simt_gemm(const SimtGemmParams& p, Epi epi, cudaStream_t s);
 cudaError_t launch_permute_ffn(const void* W1g, const void* W1u, const void* W2, const int* perm, int L, int d,
                                int F, bool bf16, void* W1g_out, void* W1u_out, void* W2_out, DeviceStatus* st,
                                int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- argument checks (api.cu)
+// Every argument check of sptp_ffn_forward_ex, with no CUDA call.
+int check_ffn_forward_args(const void* x, const void* partials, const void* gamma, const void* W1g,
+                           const void* W1u, const void* W2, int M, int d, int F, int P, int chunks, float eps,
+                           int dtype, const void* out, const void* resid_out, const void* workspace,
+                           size_t ws_bytes, int variant);
+// SPTP_OK, SPTP_ERR_DEVICE (not compute capability 10.3) or SPTP_ERR_CUDA.
+int current_device_ok();
 
 // ---------------------------------------------------------------- self-test
 cudaError_t launch_wait_selftest(DeviceStatus* st, unsigned long long limit_ns, cudaStream_t s);

@@ -62,8 +62,21 @@ def test_every_declared_function_is_documented():
 
 def test_status_strings(lib):
     assert st.sptp_status_string(0) == "ok"
-    for c in range(-1, -9, -1):
-        assert st.sptp_status_string(c) != "unknown status"
+    for name, c in st.STATUS.items():
+        assert st.sptp_status_string(c) != "unknown status", name
+    assert st.sptp_status_string(-12) == "unknown status"
+
+
+def test_status_codes_match_the_header():
+    """The binding's status and variant tables against the header's enums."""
+    src = open(os.path.join(ROOT, "include", "sptp.h")).read()
+    codes = {m.group(1).lower(): int(m.group(2)) for m in re.finditer(r"SPTP_(OK|ERR_\w+) = (-?\d+)", src)}
+    assert {k.replace("err_", ""): v for k, v in codes.items()} == st.STATUS
+    variants = {m.group(1).lower(): int(m.group(2)) for m in re.finditer(r"SPTP_VARIANT_(\w+) = (\d+)", src)}
+    assert variants == st.VARIANTS
+    # the page-given codes keep their numbers
+    assert (codes["err_null"], codes["err_shape"], codes["err_dtype"], codes["err_workspace"], codes["err_cuda"],
+            codes["err_timeout"], codes["err_unimplemented"]) == (-1, -2, -3, -4, -5, -6, -7)
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address that is never dereferenced
@@ -154,3 +167,31 @@ def test_fp8_entry_points_reject_bad_arguments(lib):
                                        FAKE * 7, FAKE * 8, 1 << 20, None) == SHAPE
     assert lib.sptp_down_proj_e4m3(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 64, 128, 512, 2, FAKE * 5, FAKE * 6, 100,
                                    None) == WS
+
+
+def test_variants_are_checked_before_any_gpu_work(lib):
+    """A variant that does not exist for an entry point or dtype is refused
+    with SPTP_ERR_UNIMPLEMENTED before any CUDA call."""
+    UNIMPL = st.STATUS["unimplemented"]
+    p = [FAKE * (i + 1) for i in range(6)]
+    ex = lambda dt, v: lib.sptp_ffn_forward_ex(*p, 64, 128, 512, 2, 4, 1e-6, dt, FAKE * 64, None, FAKE * 4096,
+                                                1 << 40, None, v)
+    V = st.VARIANTS
+    for v in (V["chain"], V["fused"], V["layers"], 9, -1):
+        assert ex(1, v) == UNIMPL, v            # fp32: PAIR only
+    for v in (V["layers"], 9):
+        assert ex(0, v) == UNIMPL, v            # bf16: no LAYERS form of the boundary
+    q = [FAKE * (i + 1) * 4096 for i in range(5)]
+    dtp = lambda dt, v: lib.dtp_ffn_stack_forward_ex(*q, 64, 128, 512, 2, 2, 1, 1, 1e-6, dt, FAKE * 64 * 4096,
+                                                      1 << 40, None, v)
+    for v in (V["pair"], V["chain"], 7):
+        assert dtp(0, v) == UNIMPL, v
+    assert dtp(1, V["fused"]) == UNIMPL
+    attn = lambda dt, v: lib.sptp_attn_qkv_forward_ex(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, 64, 128, 512, 2, 2, 1e-6,
+                                                       dt, FAKE * 64, None, FAKE * 128, 1 << 40, None, v)
+    for v in (V["chain"], V["layers"]):
+        assert attn(0, v) == UNIMPL, v
+    assert attn(1, V["fused"]) == UNIMPL
+    # the plain entry points are the AUTO forms: shape errors as before
+    assert lib.sptp_ffn_forward(*p, 64, 100, 512, 2, 4, 1e-6, 0, FAKE * 64, None, FAKE * 4096, 1 << 40,
+                                None) == st.STATUS["shape"]

@@ -103,3 +103,41 @@ def test_fp8_entry_points_check_codes_and_scales():
         st.sptp_down_proj_e4m3(z(P, M, F // P, dtype=u8), z(M, dtype=f32), z(d, F, dtype=u8), z(d, P, dtype=f32), P)
     with pytest.raises(ValueError, match="W1u"):
         st.quantize_ffn_weights_e4m3(z(F, d), z(F, d + 16), z(d, F), P)
+
+
+class OnDevice:
+    """Stands for a CUDA tensor on device `index` (shape and dtype of `t`):
+    enough for the binding's checks, which run before any pointer is taken."""
+
+    def __init__(self, t, index):
+        self.shape, self.dtype = t.shape, t.dtype
+        self.device = torch.device("cuda", index)
+
+
+def test_tensors_off_the_current_device_are_rejected_before_any_launch(monkeypatch):
+    """The library launches on the current device and takes its stream and
+    scratch from it: tensors on another device are refused by the binding,
+    before the library is called."""
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+
+    def no_library():
+        raise AssertionError("the library was called")
+    monkeypatch.setattr(st, "lib", no_library)
+    a = {k: OnDevice(v, 1) for k, v in boundary_args().items()}
+    with pytest.raises(ValueError, match="current device is cuda:0"):
+        call_ffn(a)
+    with pytest.raises(ValueError, match="current device is cuda:0"):
+        st.sptp_prologue(a["x"], a["partials"], a["gamma"], 1e-6)
+    with pytest.raises(ValueError, match="current device is cuda:0"):
+        st.sptp_ffn_forward_noalloc(a["x"], a["partials"], a["gamma"], a["W1g"], a["W1u"], a["W2"], 2, 2, 1e-6,
+                                    OnDevice(z(2, 16, 64), 1))
+    # tensors split over two devices
+    b = dict(a, W2=OnDevice(z(64, 128), 0))
+    with pytest.raises(ValueError, match="one device expected"):
+        call_ffn(b)
+
+
+def test_unknown_variant_names_are_rejected():
+    with pytest.raises(ValueError, match="unknown variant"):
+        st._variant("single")
+    assert [st._variant(v) for v in ("auto", "pair", "chain", "fused", "layers")] == [0, 1, 2, 3, 4]

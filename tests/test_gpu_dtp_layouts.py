@@ -9,16 +9,15 @@ import oracle
 import sequence_tensor_transformer_gb300 as st
 from sequence_tensor_transformer_gb300 import synth
 
-from helpers import TOL, dev_tensor, host_f64, rel_err, to_f64
+from helpers import TOL, assert_no_nan, check_errors, dev_tensor, host_f64, nan_tensor, nan_workspace, rel_err, to_f64
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(params=["fused", "layers"])
-def dtp_variant(request, monkeypatch):
+def dtp_variant(request):
     """Delayed-TP stack as one fused persistent launch (default) or as a
     prologue and two GEMM launches per module."""
-    monkeypatch.setenv("SPTP_DTP_VARIANT", request.param)
     return request.param
 
 
@@ -43,9 +42,10 @@ def test_permutation_kernel_is_exact_indexing(dtype, L, d, F):
     W1u = synth._cast(rng.standard_normal((L, F, d)), dtype)
     W2 = synth._cast(rng.standard_normal((L, d, F)), dtype)
     perm = _perms(L, F, 5)
+    hdr = nan_workspace(st.SPTP_WS_HEADER_BYTES)
     outs = st.sptp_permute_ffn_neurons(dev_tensor(W1g, dtype), dev_tensor(W1u, dtype), dev_tensor(W2, dtype),
-                                       torch.from_numpy(perm).cuda())
-    torch.cuda.synchronize()
+                                       torch.from_numpy(perm).cuda(), workspace=hdr)
+    assert st.sptp_read_device_status(hdr) == 0
     view = (lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)) if dtype == "bf16" else \
         (lambda t: t.cpu().numpy())
     for l in range(L):
@@ -70,12 +70,17 @@ def test_out_of_range_index_is_reported_and_zero_filled():
     assert torch.equal(g[0, 4], W[0][0, 4]) and torch.equal(w2[0][:, 4], W2[0][:, 4])
 
 
-def run_permuted_dtp(cfg, perms, flush, rows=None):
+def run_permuted_dtp(cfg, perms, flush, rows=None, variant="auto"):
     inp = synth.dtp_inputs(cfg)
     T = {k: dev_tensor(v, cfg.dtype) for k, v in inp.items()}
-    g, u, w2 = st.sptp_permute_ffn_neurons(T["W1g"], T["W1u"], T["W2"], torch.from_numpy(perms).cuda())
-    st.dtp_ffn_stack_forward(T["x_shards"], T["gamma"], g, u, w2, cfg.P, cfg.L, cfg.delta, flush, cfg.eps)
-    torch.cuda.synchronize()
+    hdr = nan_workspace(st.SPTP_WS_HEADER_BYTES)
+    g, u, w2 = st.sptp_permute_ffn_neurons(T["W1g"], T["W1u"], T["W2"], torch.from_numpy(perms).cuda(), workspace=hdr)
+    assert st.sptp_read_device_status(hdr) == 0
+    ws = nan_workspace(st.dtp_ffn_stack_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.L, cfg.delta, st.SPTP_BF16))
+    st.dtp_ffn_stack_forward(T["x_shards"], T["gamma"], g, u, w2, cfg.P, cfg.L, cfg.delta, flush, cfg.eps,
+                             workspace=ws, variant=variant)
+    assert st.sptp_read_device_status(ws) == 0
+    assert_no_nan(T["x_shards"])
     f64 = {k: to_f64(v, cfg.dtype) for k, v in inp.items()}
     xs = f64["x_shards"] if rows is None else f64["x_shards"][:, rows]
     ref = oracle.dtp_ffn_stack_forward_permuted(xs, f64["gamma"], f64["W1g"], f64["W1u"], f64["W2"], perms,
@@ -87,14 +92,12 @@ def run_permuted_dtp(cfg, perms, flush, rows=None):
 def test_permuted_dtp_stack_workload_sampled_rows(dtp_variant):
     cfg = synth.DTP_STACK
     rows = [0, 1, 77, 1024, 2047, 3333, 4095]
-    got, ref = run_permuted_dtp(cfg, _perms(cfg.L, cfg.F, 11), 1, rows=rows)
-    for p in range(cfg.P):
-        assert rel_err(got[p], ref[p]) <= TOL["bf16"]
+    got, ref = run_permuted_dtp(cfg, _perms(cfg.L, cfg.F, 11), 1, rows=rows, variant=dtp_variant)
+    check_errors({p: rel_err(got[p], ref[p]) for p in range(cfg.P)}, "bf16")
 
 
 @pytest.mark.parametrize("P,L,delta,flush", [(2, 3, 1, 0), (3, 2, 0, 1), (4, 3, 2, 1)])
 def test_permuted_dtp_small_cases(P, L, delta, flush, dtp_variant):
     cfg = synth.DTPConfig("perm", 160, 136, P * 48, P, L, delta, "bf16")
-    got, ref = run_permuted_dtp(cfg, _perms(L, cfg.F, P + L), flush)
-    for p in range(P):
-        assert rel_err(got[p], ref[p]) <= TOL["bf16"]
+    got, ref = run_permuted_dtp(cfg, _perms(L, cfg.F, P + L), flush, variant=dtp_variant)
+    check_errors({p: rel_err(got[p], ref[p]) for p in range(P)}, "bf16")
