@@ -21,7 +21,7 @@ __all__ = [
     "sptp_attn_qkv_workspace_size", "sptp_attn_qkv_forward", "sptp_quantize_rows_e4m3",
     "quantize_ffn_weights_e4m3", "sptp_ffn_fp8_workspace_size", "sptp_ffn_forward_fp8",
     "sptp_gateup_swiglu_e4m3", "sptp_down_proj_e4m3", "sptp_prologue_e4m3", "VARIANTS", "STATUS",
-    "sptp_noalloc_read_device_status", "sptp_noalloc_wait_selftest",
+    "sptp_noalloc_read_device_status", "sptp_noalloc_wait_selftest", "CHECKED_LIB_PATH", "set_library",
 ]
 
 SPTP_BF16 = 0
@@ -85,10 +85,15 @@ class SptpError(RuntimeError):
         self.code = code
 
 
-def load_library(path: str = LIB_PATH):
-    """Loads libsptp.so (built by sequence_tensor_transformer_gb300.build)."""
+CHECKED_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsptp_check.so")
+
+
+def load_library(path: str = LIB_PATH, replace: bool = False):
+    """Loads libsptp.so (built by sequence_tensor_transformer_gb300.build) on
+    first use.  replace=True makes `path` the library every later call uses:
+    for example CHECKED_LIB_PATH, the bounds-checked build (build(checked=True))."""
     global _lib
-    if _lib is None:
+    if _lib is None or replace:
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is missing: build it with "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
@@ -99,6 +104,12 @@ def load_library(path: str = LIB_PATH):
             f.argtypes = args
         _lib = lib_
     return _lib
+
+
+def set_library(handle):
+    """Makes a handle returned by load_library the one every call uses."""
+    global _lib
+    _lib = handle
 
 
 def lib():

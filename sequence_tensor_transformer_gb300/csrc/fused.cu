@@ -98,6 +98,16 @@ __device__ __forceinline__ Tile decode(const FusedParams& p, int t) {
     return r;
 }
 
+// A checked build: the decoded tile lies in the launch's tile grid.
+__device__ __forceinline__ bool tile_ok(const FusedParams& p, const Tile& tl, volatile int* abort_flag) {
+    if constexpr (kBoundsChecked) {
+        const int nt = tl.down ? p.nt_dn : p.nt_gu;
+        const bool ok = tl.g >= 0 && tl.g < p.P && tl.m >= 0 && tl.m < p.mt && tl.n >= 0 && tl.n < nt;
+        return checked(ok, p.status, abort_flag, kWhereBoundsTile, static_cast<long long>(tl.m) * 65536 + tl.n);
+    }
+    return true;
+}
+
 // silu with the fast divide (<= 2 ulp in fp32, below the bf16 output rounding)
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
@@ -195,7 +205,8 @@ __device__ __forceinline__ void row_h(const FusedParams& p, long long row_off, i
 constexpr int kBrSrc = 5;  // sources held at once: P + 1 <= 5
 constexpr int kBrVec = 2;  // vectors per thread: d <= 2 * 8 * 32 * PRO_WARPS
 
-__device__ __forceinline__ void prologue_block_rows(const FusedParams& p, int tid, int wp, int lane) {
+__device__ __forceinline__ void prologue_block_rows(const FusedParams& p, int tid, int wp, int lane,
+                                                    volatile int* abort_flag) {
     constexpr int NT = 32 * PRO_WARPS;
     __shared__ float red[2][kBrVec * PRO_WARPS];
     const int d = p.d;
@@ -205,8 +216,12 @@ __device__ __forceinline__ void prologue_block_rows(const FusedParams& p, int ti
     for (int k = 0; k < kBrVec; ++k)
         if (tid + k * NT < nvec) load8(static_cast<const __nv_bfloat16*>(p.gamma) + (tid + k * NT) * 8, gm[k]);
     int par = 0;
+    const long long md = static_cast<long long>(p.M) * d;
     for (long long row = blockIdx.x; row < p.M; row += gridDim.x) {
         const long long base = row * d;
+        // a checked build: every vector of the row inside [M][d] (a failed
+        // check leaves the whole row out, in every thread of the CTA alike)
+        if (!checked_range(base, d, md, p.status, abort_flag, kWhereBoundsLoad)) break;
         uint4 u[kBrSrc][kBrVec];
 #pragma unroll
         for (int q = 0; q < kBrSrc; ++q) {
@@ -268,7 +283,8 @@ __device__ __forceinline__ void prologue_block_rows(const FusedParams& p, int ti
         // make this warp's part of y visible to the TMA loads of other CTAs
         fence_proxy_async_global();
         __syncwarp();
-        if (lane == 0) red_release_add(&p.chunk_ready[row / p.chunk_rows], 1);
+        if (lane == 0 && checked_index(row / p.chunk_rows, p.chunks, p.status, abort_flag, kWhereBoundsCounter))
+            red_release_add(&p.chunk_ready[row / p.chunk_rows], 1);
     }
 }
 
@@ -296,6 +312,9 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
         }
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
+        // a checked build: the launch is a cluster of two CTAs (every peer
+        // address below maps into CTA 0 or 1 of it)
+        checked(cluster_nctarank() == 2 && rank < 2, p.status, &bars->abort_flag, kWhereBoundsCluster, rank);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -319,15 +338,18 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
     const uint32_t tmem_base = bars->tmem_base;
 
     WaitCtx wc{p.status, &bars->abort_flag, p.wait_limit_ns};
-    const int total = p.tiles_gu + p.tiles_dn;
+    volatile int* abort_flag = &bars->abort_flag;
+    // false only in a checked build whose cluster check failed: no role runs
+    const bool cta_ok = bars->abort_flag == 0;
+    const int total = cta_ok ? p.tiles_gu + p.tiles_dn : 0;
     const int pair_id = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
 
-    if (warp >= 6 && p.pre_normed) {
+    if ((warp >= 6 && p.pre_normed) || (warp >= 6 && !cta_ok)) {
         // y is already written: nothing for the prologue warps to do
     } else if (warp >= 6 && p.block_rows) {
         // ------------------------------------------------ prologue rows, one per CTA at a time
-        prologue_block_rows(p, threadIdx.x - 6 * 32, warp - 6, lane);
+        prologue_block_rows(p, threadIdx.x - 6 * 32, warp - 6, lane, abort_flag);
     } else if (warp >= 6) {
         // ------------------------------------------------ prologue rows, one per warp
         const int W = gridDim.x * PRO_WARPS;
@@ -335,6 +357,8 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
         for (long long row = static_cast<long long>(blockIdx.x) * PRO_WARPS + (warp - 6); row < p.M; row += W) {
             if (*wc.abort_flag) break;
             const long long base = row * d;
+            if (!checked_range(base, d, static_cast<long long>(p.M) * d, p.status, abort_flag, kWhereBoundsLoad))
+                break;
             constexpr int NV = 4;
             float ss = 0.f;
             for (int col0 = lane * 8; col0 < d; col0 += 256 * NV) {
@@ -369,7 +393,8 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             // make the row's y visible to the TMA loads of other CTAs
             fence_proxy_async_global();
             __syncwarp();
-            if (lane == 0) red_release_add(&p.chunk_ready[row / p.chunk_rows], 1);
+            if (lane == 0 && checked_index(row / p.chunk_rows, p.chunks, p.status, abort_flag, kWhereBoundsCounter))
+                red_release_add(&p.chunk_ready[row / p.chunk_rows], 1);
         }
     } else if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -381,6 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
         bool ok = true;
         for (int t = pair_id; ok && t < total; t += npairs) {
             const Tile tl = decode(p, t);
+            if (!tile_ok(p, tl, abort_flag)) break;
             // dependency of this tile's A operand
             if (!tl.down) {
                 if (!p.pre_normed) {
@@ -389,10 +415,12 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     const int need = p.chunk_rows * (p.block_rows ? PRO_WARPS : 1);
                     const int c1 = (min(p.M, (tl.m + 1) * PBM) - 1) / p.chunk_rows;
                     for (int c = tl.m * PBM / p.chunk_rows; ok && c <= c1; ++c)
-                        ok = flag_wait_geq(&p.chunk_ready[c], need, wc, kWhereFusedRows, t);
+                        ok = checked_index(c, p.chunks, p.status, abort_flag, kWhereBoundsCounter) &&
+                             flag_wait_geq(&p.chunk_ready[c], need, wc, kWhereFusedRows, t);
                 }
             } else {
-                ok = flag_wait_geq(&p.gu_done[tl.g * p.mt + tl.m], 2 * p.nt_gu, wc, kWhereFusedGateUp, t);
+                ok = checked_index(tl.g * p.mt + tl.m, p.P * p.mt, p.status, abort_flag, kWhereBoundsCounter) &&
+                     flag_wait_geq(&p.gu_done[tl.g * p.mt + tl.m], 2 * p.nt_gu, wc, kWhereFusedGateUp, t);
             }
             if (!ok) break;
             fence_proxy_async_global();
@@ -404,7 +432,17 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             const CUtensorMap* mB =
                 tl.down ? &p.mapW2[tl.g] : (p.qkv || rank == 0 ? &p.mapW1g[tl.g] : &p.mapW1u[tl.g]);
             const int brow = split_b ? tl.n * PBN + static_cast<int>(rank) * 128 : tl.n * 128;
+            const int arow = tl.m * PBM + static_cast<int>(rank) * 128;
+            // a checked build: the box origins of every k-block (A: y [M][d]
+            // or s [M][f]; B: W1g/W1u/Wqkv rows [f][d] or W2 columns [d][f])
+            const int ka = tl.down ? p.f : p.d;
+            const int b_rows = tl.down ? p.nt_dn * PBN : (p.qkv ? p.nt_gu * PBN : p.nt_gu * 128);
             for (int kb = 0; kb < nk; ++kb) {
+                if (!checked_tma(kb * BK, BK, ka, arow, static_cast<long long>(p.mt) * PBM, p.status, abort_flag) ||
+                    !checked_tma(kb * BK, BK, ka, brow, b_rows, p.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 if (!mbar_wait(&bars->empty[stage], phase ^ 1u, wc, kWhereProducerEmpty, t)) {
                     ok = false;
                     break;
@@ -414,7 +452,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     armed_parity[stage] = static_cast<int>(phase);
                 }
                 const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
-                tma_load_2d_pair(a_tiles + stage * A_BYTES, mA, fb, kb * BK, tl.m * PBM + static_cast<int>(rank) * 128);
+                tma_load_2d_pair(a_tiles + stage * A_BYTES, mA, fb, kb * BK, arow);
                 tma_load_2d_pair(b_tiles + stage * B_BYTES, mB, fb, kb * BK, brow);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -441,6 +479,7 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
         int local = 0;
         for (int t = pair_id; ok && t < total; t += npairs, ++local) {
             const Tile tl = decode(p, t);
+            if (!tile_ok(p, tl, abort_flag)) break;
             const int nk = tl.down ? p.nk_dn : p.nk_gu;
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
@@ -486,8 +525,11 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
             if (epilogue_any(!ok)) break;
             tc_fence_after();
             const Tile tl = decode(p, t);
+            // a checked build: a bad tile leaves it unstored (its readers
+            // then give up through their bounded waits)
+            const bool tile_good = tile_ok(p, tl, abort_flag);
             const int row = tl.m * PBM + row_in_tile;
-            const bool row_ok = row < p.M;
+            const bool row_ok = row < p.M && tile_good;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
             if (!tl.down && !p.qkv) {
@@ -510,7 +552,10 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     if (row_ok) {
 #pragma unroll
                         for (int v = 0; v < 2; ++v)
-                            if (col + 8 * v < p.f)
+                            if (col + 8 * v < p.f &&
+                                checked_range(static_cast<long long>(row) * p.f + col + 8 * v, 8,
+                                              static_cast<long long>(p.M) * p.f, p.status, abort_flag,
+                                              kWhereBoundsStore))
                                 *reinterpret_cast<uint4*>(out + col + 8 * v) =
                                     make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
                     }
@@ -533,7 +578,10 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                     if (row_ok) {
 #pragma unroll
                         for (int v = 0; v < 2; ++v)
-                            if (col + 8 * v < ncols)
+                            if (col + 8 * v < ncols &&
+                                checked_range(static_cast<long long>(row) * ncols + col + 8 * v, 8,
+                                              static_cast<long long>(p.M) * ncols, p.status, abort_flag,
+                                              kWhereBoundsStore))
                                 __stcs(reinterpret_cast<uint4*>(out + col + 8 * v),
                                        make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
                                                   packed[4 * v + 3]));
@@ -548,7 +596,9 @@ __global__ void __launch_bounds__(THREADS, 1) boundary_fused_kernel(const __grid
                 // to the down tiles' TMA loads
                 fence_proxy_async_global();
                 named_barrier_sync<1, 128>();
-                if (warp == 2 && lane == 0) red_release_add(&p.gu_done[tl.g * p.mt + tl.m], 1);
+                if (warp == 2 && lane == 0 && tile_good &&
+                    checked_index(tl.g * p.mt + tl.m, p.P * p.mt, p.status, abort_flag, kWhereBoundsCounter))
+                    red_release_add(&p.gu_done[tl.g * p.mt + tl.m], 1);
             }
         }
     }

@@ -115,6 +115,17 @@ __device__ __forceinline__ Tile decode(const DtpFusedParams& p, int t) {
     return r;
 }
 
+// A checked build: the decoded tile lies in the launch's tile grid.
+__device__ __forceinline__ bool tile_ok(const DtpFusedParams& p, const Tile& tl, volatile int* abort_flag) {
+    if constexpr (kBoundsChecked) {
+        const int nt = tl.down ? p.nt_dn : p.nt_gu;
+        const bool ok = tl.l >= 0 && tl.l < p.L && tl.m >= 0 && tl.m < p.mt && tl.p >= 0 && tl.p < p.P && tl.n >= 0 &&
+                        tl.n < nt;
+        return checked(ok, p.status, abort_flag, kWhereBoundsTile, static_cast<long long>(tl.m) * 65536 + tl.n);
+    }
+    return true;
+}
+
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -162,7 +173,8 @@ __device__ __forceinline__ int n_sources(const DtpFusedParams& p, int l) {
     return n;
 }
 
-__device__ __forceinline__ const __nv_bfloat16* source_j(const DtpFusedParams& p, int l, int sh, int j) {
+__device__ __forceinline__ const __nv_bfloat16* source_j(const DtpFusedParams& p, int l, int sh, int j,
+                                                         volatile int* abort_flag) {
     const long long act = static_cast<long long>(p.M) * p.d;
     const __nv_bfloat16* ring = static_cast<const __nv_bfloat16*>(p.ring);
     int module, q;
@@ -183,6 +195,12 @@ __device__ __forceinline__ const __nv_bfloat16* source_j(const DtpFusedParams& p
         }
         q = idx < sh ? idx : idx + 1;
     }
+    // a checked build: a module that has run, one of the P shards, and the
+    // ring slot it lives in
+    if (!checked_index(module, p.L, p.status, abort_flag, kWhereBoundsRing) ||
+        !checked_index(q, p.P, p.status, abort_flag, kWhereBoundsRing) ||
+        !checked_index(module % p.S, p.S, p.status, abort_flag, kWhereBoundsRing))
+        return nullptr;
     return ring + (static_cast<long long>(module % p.S) * p.P + q) * act;
 }
 
@@ -193,7 +211,7 @@ __device__ __forceinline__ const __nv_bfloat16* source_j(const DtpFusedParams& p
 constexpr int kSrcBatch = 3;
 
 __device__ __forceinline__ void step_h(const DtpFusedParams& p, int l, int sh, long long row, int base, int lane,
-                                       float (&h)[kRowVec][8]) {
+                                       float (&h)[kRowVec][8], volatile int* abort_flag) {
     const long long act = static_cast<long long>(p.M) * p.d;
     const long long off = row * p.d + base + lane * 8;
     const int col0 = base + lane * 8;
@@ -208,11 +226,15 @@ __device__ __forceinline__ void step_h(const DtpFusedParams& p, int l, int sh, l
         for (int jj = 0; jj < kSrcBatch; ++jj) {
             const int j = j0 + jj;
             if (j <= ns) {
-                const __nv_bfloat16* src =
-                    (j == ns ? static_cast<const __nv_bfloat16*>(p.x) + sh * act : source_j(p, l, sh, j)) + off;
+                const __nv_bfloat16* s0 =
+                    j == ns ? static_cast<const __nv_bfloat16*>(p.x) + sh * act : source_j(p, l, sh, j, abort_flag);
 #pragma unroll
-                for (int v = 0; v < kRowVec; ++v)
-                    if (col0 + 256 * v < p.d) u[jj][v] = *reinterpret_cast<const uint4*>(src + 256 * v);
+                for (int v = 0; v < kRowVec; ++v) {
+                    u[jj][v] = make_uint4(0u, 0u, 0u, 0u);
+                    if (col0 + 256 * v < p.d && s0 != nullptr &&
+                        checked_range(off + 256 * v, 8, act, p.status, abort_flag, kWhereBoundsLoad))
+                        u[jj][v] = *reinterpret_cast<const uint4*>(s0 + off + 256 * v);
+                }
             }
         }
         // in order: the sources, then x (one IEEE addition each, so h + x ==
@@ -239,7 +261,7 @@ __device__ __forceinline__ void step_h(const DtpFusedParams& p, int l, int sh, l
 
 // Writes one batch of the row: x_p <- h, and y_p <- h * inv * gamma_l (l < L).
 __device__ __forceinline__ void step_store(const DtpFusedParams& p, int l, int sh, long long row, int base, int lane,
-                                           const float (&h)[kRowVec][8], float inv) {
+                                           const float (&h)[kRowVec][8], float inv, volatile int* abort_flag) {
     const long long act = static_cast<long long>(p.M) * p.d;
     __nv_bfloat16* xr = static_cast<__nv_bfloat16*>(p.x) + sh * act + row * p.d;
     __nv_bfloat16* yr = static_cast<__nv_bfloat16*>(p.y) + sh * act + row * p.d;
@@ -247,7 +269,9 @@ __device__ __forceinline__ void step_store(const DtpFusedParams& p, int l, int s
 #pragma unroll
     for (int v = 0; v < kRowVec; ++v) {
         const int col = base + lane * 8 + 256 * v;
-        if (col < p.d) {
+        // a checked build: x_p and y_p are [P][M][d]
+        if (col < p.d && checked_range(sh * act + row * p.d + col, 8, p.P * act, p.status, abort_flag,
+                                       kWhereBoundsStore)) {
             if (l < p.L) {
                 float gm[8];
 #pragma unroll
@@ -287,6 +311,8 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
         }
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
+        // a checked build: the launch is a cluster of two CTAs
+        checked(cluster_nctarank() == 2 && rank < 2, p.status, &bars->abort_flag, kWhereBoundsCluster, rank);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -307,11 +333,14 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
     const uint32_t tmem_base = bars->tmem_base;
 
     WaitCtx wc{p.status, &bars->abort_flag, p.wait_limit_ns};
-    const int total = p.total_tiles;
+    volatile int* abort_flag = &bars->abort_flag;
+    // false only in a checked build whose cluster check failed: no role runs
+    const bool cta_ok = bars->abort_flag == 0;
+    const int total = cta_ok ? p.total_tiles : 0;
     const int pair_id = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
 
-    if (warp >= PRO_WARP0) {
+    if (warp >= PRO_WARP0 && cta_ok) {
         // ------------------------------------------------ prologue rows, all steps
         // 32-bit row numbering (P * M * (L + 1) < 2^31, checked at launch):
         // 64-bit divisions per row would cost the warps more than the row
@@ -330,6 +359,10 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
             const uint32_t idx = rem - static_cast<uint32_t>(m) * per_block;
             const int sh = static_cast<int>(rows_m == PBM ? idx / PBM : idx / static_cast<uint32_t>(rows_m));
             const long long row = static_cast<long long>(m) * PBM + (idx - static_cast<uint32_t>(sh) * rows_m);
+            // a checked build: the row's (step, block, shard, row) and its counters
+            if (!checked(l <= p.L && m < p.mt && sh < p.P && row < p.M, p.status, abort_flag, kWhereBoundsTile, i) ||
+                !checked_index(l * p.mt + m, (p.L + 1) * p.mt, p.status, abort_flag, kWhereBoundsCounter))
+                break;
             if (l >= 1 &&
                 !warp_flag_wait_geq(&p.dn_done[(l - 1) * p.mt + m], 2 * p.P * p.nt_dn, wc, kWhereFusedRows,
                                     static_cast<int>(i)))
@@ -337,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
             float ss = 0.f;
             float h[kRowVec][8];
             for (int base = 0; base < d; base += 256 * kRowVec) {
-                step_h(p, l, sh, row, base, lane, h);
+                step_h(p, l, sh, row, base, lane, h, abort_flag);
 #pragma unroll
                 for (int v = 0; v < kRowVec; ++v)
                     if (base + lane * 8 + 256 * v < d)
@@ -348,11 +381,11 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
             const float inv = rsqrtf(ss / static_cast<float>(d) + p.eps);
             __syncwarp();  // every lane has read x_p[row] before it is rewritten
             if (d <= 256 * kRowVec) {
-                step_store(p, l, sh, row, 0, lane, h, inv);  // one batch: h is still in registers
+                step_store(p, l, sh, row, 0, lane, h, inv, abort_flag);  // one batch: h is still in registers
             } else {
                 for (int base = 0; base < d; base += 256 * kRowVec) {
-                    step_h(p, l, sh, row, base, lane, h);  // same inputs and order: the same h
-                    step_store(p, l, sh, row, base, lane, h, inv);
+                    step_h(p, l, sh, row, base, lane, h, abort_flag);  // same inputs and order: the same h
+                    step_store(p, l, sh, row, base, lane, h, inv, abort_flag);
                 }
             }
             if (l < p.L) {
@@ -372,18 +405,33 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
         bool ok = true;
         for (int t = pair_id; ok && t < total; t += npairs) {
             const Tile tl = decode(p, t);
+            if (!tile_ok(p, tl, abort_flag)) break;
             if (!tl.down) {
                 const int need = p.P * min(PBM, p.M - tl.m * PBM);
-                ok = flag_wait_geq(&p.rb_ready[tl.l * p.mt + tl.m], need, wc, kWhereFusedRows, t);
+                ok = checked_index(tl.l * p.mt + tl.m, p.L * p.mt, p.status, abort_flag, kWhereBoundsCounter) &&
+                     flag_wait_geq(&p.rb_ready[tl.l * p.mt + tl.m], need, wc, kWhereFusedRows, t);
             } else {
-                ok = flag_wait_geq(&p.gu_done[(tl.l * p.P + tl.p) * p.mt + tl.m], 2 * p.nt_gu, wc,
-                                   kWhereFusedGateUp, t);
+                const int gi = (tl.l * p.P + tl.p) * p.mt + tl.m;
+                ok = checked_index(gi, p.L * p.P * p.mt, p.status, abort_flag, kWhereBoundsCounter) &&
+                     flag_wait_geq(&p.gu_done[gi], 2 * p.nt_gu, wc, kWhereFusedGateUp, t);
             }
             if (!ok) break;
             fence_proxy_async_global();
             const int nk = tl.down ? p.nk_dn : p.nk_gu;
             const int arow = tl.m * PBM + static_cast<int>(rank) * 128;
+            // B rows: gate/up tiles n * 128 of [f] rows; down tiles n * 256 +
+            // rank * 128 of [d] rows
+            const int brow = tl.down ? tl.n * PBN + static_cast<int>(rank) * 128 : tl.n * 128;
+            const int b_rows = tl.down ? p.nt_dn * PBN : p.nt_gu * 128;
+            const int ka = tl.down ? p.f : p.d;
             for (int kb = 0; kb < nk; ++kb) {
+                // a checked build: the box origins (the trailing coordinates,
+                // shard and module, are checked with the tile)
+                if (!checked_tma(kb * BK, BK, ka, arow, static_cast<long long>(p.mt) * PBM, p.status, abort_flag) ||
+                    !checked_tma(kb * BK, BK, ka, brow, b_rows, p.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 if (!mbar_wait(&bars->empty[stage], phase ^ 1u, wc, kWhereProducerEmpty, t)) {
                     ok = false;
                     break;
@@ -397,12 +445,10 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
                 uint8_t* bt = b_tiles + stage * B_BYTES;
                 if (!tl.down) {
                     tma_load_3d_pair(at, &p.mapY, fb, kb * BK, arow, tl.p);
-                    tma_load_3d_pair(bt, rank == 0 ? &p.mapW1g : &p.mapW1u, fb, kb * BK, tl.n * 128,
-                                     tl.l * p.P + tl.p);
+                    tma_load_3d_pair(bt, rank == 0 ? &p.mapW1g : &p.mapW1u, fb, kb * BK, brow, tl.l * p.P + tl.p);
                 } else {
                     tma_load_3d_pair(at, &p.mapS, fb, kb * BK, arow, tl.p);
-                    tma_load_4d_pair(bt, &p.mapW2, fb, kb * BK, tl.p, tl.n * PBN + static_cast<int>(rank) * 128,
-                                     tl.l);
+                    tma_load_4d_pair(bt, &p.mapW2, fb, kb * BK, tl.p, brow, tl.l);
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -429,6 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
         int local = 0;
         for (int t = pair_id; ok && t < total; t += npairs, ++local) {
             const Tile tl = decode(p, t);
+            if (!tile_ok(p, tl, abort_flag)) break;
             const int nk = tl.down ? p.nk_dn : p.nk_gu;
             const int acc = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
@@ -477,7 +524,12 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
             if (named_barrier_any<1, 32 * EPI_WARPS>(!ok)) break;
             tc_fence_after();
             const Tile tl = decode(p, t);
-            const int row0 = tl.m * PBM + static_cast<int>(rank) * 128 + quarter * 32;  // the warp's first row
+            // a checked build: a bad tile or ring slot is not stored (its
+            // readers then give up through their bounded waits)
+            const bool tile_good = tile_ok(p, tl, abort_flag) &&
+                                   checked_index(tl.l % p.S, p.S, p.status, abort_flag, kWhereBoundsRing);
+            const int row0 = tile_good ? tl.m * PBM + static_cast<int>(rank) * 128 + quarter * 32
+                                       : p.M;  // the warp's first row
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * PBN);
             uint8_t* wbuf = out_stage + (warp - 2) * kOutWarpBytes;
@@ -501,7 +553,8 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
                         }
                     }
                     store_block_staged<false>(wbuf, packed, lane, out, p.f, nullptr, 0, 0, row0, p.M,
-                                              tl.n * (PBN / 2) + c0, p.f);
+                                              tl.n * (PBN / 2) + c0, p.f, static_cast<long long>(p.M) * p.f,
+                                              p.status, abort_flag);
                 }
             } else {
                 // the partial [M][d] in ring slot l mod S, shard p, in blocks of 64 columns
@@ -521,7 +574,7 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
                                 pack_bf16x2(__uint_as_float(v16[2 * j]), __uint_as_float(v16[2 * j + 1]));
                     }
                     store_block_staged<false>(wbuf, packed, lane, out, p.d, nullptr, 0, 0, row0, p.M,
-                                              tl.n * PBN + c0, p.d);
+                                              tl.n * PBN + c0, p.d, act, p.status, abort_flag);
                 }
             }
             // reads complete and fenced; outputs are published separately below
@@ -532,11 +585,14 @@ __global__ void __launch_bounds__(THREADS, 1) dtp_fused_kernel(const __grid_cons
             // next steps' prologue rows, plain loads: release/acquire suffices)
             if (!tl.down) fence_proxy_async_global();
             named_barrier_sync<1, 32 * EPI_WARPS>();
-            if (warp == 2 && lane == 0) {
-                if (!tl.down)
-                    red_release_add(&p.gu_done[(tl.l * p.P + tl.p) * p.mt + tl.m], 1);
-                else
+            if (warp == 2 && lane == 0 && tile_good) {
+                if (!tl.down) {
+                    const int gi = (tl.l * p.P + tl.p) * p.mt + tl.m;
+                    if (checked_index(gi, p.L * p.P * p.mt, p.status, abort_flag, kWhereBoundsCounter))
+                        red_release_add(&p.gu_done[gi], 1);
+                } else if (checked_index(tl.l * p.mt + tl.m, p.L * p.mt, p.status, abort_flag, kWhereBoundsCounter)) {
                     red_release_add(&p.dn_done[tl.l * p.mt + tl.m], 1);
+                }
             }
         }
     }

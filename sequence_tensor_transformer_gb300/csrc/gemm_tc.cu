@@ -122,6 +122,15 @@ __device__ __forceinline__ void load_col_scales_strided(const float* sc, int str
     for (int j = 0; j < 32; ++j) cs[j] = col + j < N ? __ldg(sc + static_cast<long long>(col + j) * stride) : 0.0f;
 }
 
+// A checked build: the decoded tile lies in the launch's tile grid.
+__device__ __forceinline__ bool tile_ok(const TcGemmParams& p, int g, int m, int n, volatile int* abort_flag) {
+    if constexpr (kBoundsChecked) {
+        const bool ok = g >= 0 && g < p.G && m >= 0 && m < p.mt && n >= 0 && n < p.nt;
+        return checked(ok, p.status, abort_flag, kWhereBoundsTile, static_cast<long long>(m) * 65536 + n);
+    }
+    return true;
+}
+
 struct Bars {
     uint64_t full[kMaxPStages];
     uint64_t empty[kMaxPStages];
@@ -160,6 +169,8 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
         }
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
+        // a checked build: the launch is a cluster of two CTAs
+        checked(cluster_nctarank() == 2 && rank < 2, p.status, &bars->abort_flag, kWhereBoundsCluster, rank);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -180,7 +191,9 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
     const uint32_t tmem_base = bars->tmem_base;
 
     WaitCtx wc{p.status, &bars->abort_flag, p.wait_limit_ns};
-    const int total = p.G * p.mt * p.nt;
+    volatile int* abort_flag = &bars->abort_flag;
+    // zero only in a checked build whose cluster check failed: no role runs
+    const int total = bars->abort_flag == 0 ? p.G * p.mt * p.nt : 0;
     const int pair_id = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
 
@@ -195,7 +208,17 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
         for (int t = pair_id; ok && t < total; t += npairs) {
             int g, m, n;
             decode_tile(p, t, g, m, n);
+            if (!tile_ok(p, g, m, n, abort_flag)) break;
+            const int arow = m * PBM + static_cast<int>(rank) * 128;
+            const int brow = EPI == Epi::kSwiGLU ? n * 128 : n * PBN + static_cast<int>(rank) * 128;
+            const int b_rows = EPI == Epi::kSwiGLU ? p.nt * 128 : p.nt * PBN;
             for (int kb = 0; kb < p.nk; ++kb) {
+                // a checked build: the box origins of both operands
+                if (!checked_tma(kb * KE, KE, p.K, arow, static_cast<long long>(p.mt) * PBM, p.status, abort_flag) ||
+                    !checked_tma(kb * KE, KE, p.K, brow, b_rows, p.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 if (!mbar_wait(&bars->empty[stage], phase ^ 1u, wc, kWhereProducerEmpty, t)) {
                     ok = false;
                     break;
@@ -205,13 +228,12 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                     armed_parity[stage] = static_cast<int>(phase);
                 }
                 const uint32_t fb = full0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
-                tma_load_2d_pair(a_tiles + stage * A_BYTES, &p.mapA[g], fb, kb * KE,
-                                 m * PBM + static_cast<int>(rank) * 128);
+                tma_load_2d_pair(a_tiles + stage * A_BYTES, &p.mapA[g], fb, kb * KE, arow);
                 uint8_t* bt = b_tiles + stage * B_BYTES;
                 if (EPI == Epi::kSwiGLU) {
-                    tma_load_2d_pair(bt, rank == 0 ? &p.mapB0[g] : &p.mapB1[g], fb, kb * KE, n * 128);
+                    tma_load_2d_pair(bt, rank == 0 ? &p.mapB0[g] : &p.mapB1[g], fb, kb * KE, brow);
                 } else {
-                    tma_load_2d_pair(bt, &p.mapB0[g], fb, kb * KE, n * PBN + static_cast<int>(rank) * 128);
+                    tma_load_2d_pair(bt, &p.mapB0[g], fb, kb * KE, brow);
                 }
                 if (++stage == PSTAGES) {
                     stage = 0;
@@ -292,7 +314,10 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
             tc_fence_after();
             int g, m, n;
             decode_tile(p, t, g, m, n);
-            const int row0 = m * PBM + static_cast<int>(rank) * 128 + quarter * 32;  // the warp's first row
+            // a checked build: a bad tile is not stored
+            const bool tile_good = tile_ok(p, g, m, n, abort_flag);
+            if (!tile_good) g = 0;
+            const int row0 = tile_good ? m * PBM + static_cast<int>(rank) * 128 + quarter * 32 : p.M;
             const int row = row0 + lane;
             const bool row_ok = row < p.M;
             const uint32_t taddr =
@@ -331,7 +356,10 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                     if (row_ok) {
 #pragma unroll
                         for (int v = 0; v < 4; ++v)
-                            if (col + 8 * v < p.N)
+                            if (col + 8 * v < p.N &&
+                                checked_range(static_cast<long long>(row) * p.ldo + col + 8 * v, 8,
+                                              static_cast<long long>(p.M) * p.ldo, p.status, abort_flag,
+                                              kWhereBoundsStore))
                                 *reinterpret_cast<uint4*>(orow + col + 8 * v) =
                                     make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
                     }
@@ -362,8 +390,10 @@ __global__ void __launch_bounds__(pair_threads<EW>(), 1) tc_gemm_pair_kernel(con
                         }
                     }
                     // the outputs are final: evict-first stores
+                    const long long limit = p.split_w > 0 ? static_cast<long long>(p.N / p.split_w) * p.split_stride
+                                                          : static_cast<long long>(p.M) * p.ldo;
                     store_block_staged<true>(wbuf, packed, lane, out, p.ldo, split_out, p.split_w, p.split_stride,
-                                             row0, p.M, n * PBN + c0, p.N);
+                                             row0, p.M, n * PBN + c0, p.N, limit, p.status, abort_flag);
                 }
             }
             // The accumulator's reads are complete (tcgen05.wait::ld) and

@@ -16,6 +16,7 @@
 
 #include "sptp.h"
 #include "sptp_internal.h"
+#include "sptp_ptx.cuh"
 
 namespace sptp {
 
@@ -44,7 +45,12 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint8_t* in0, c
         const long long mat = static_cast<long long>(l) * F * row_bytes;
         const long long dst_off = mat + (w - static_cast<long long>(l) * F) * row_bytes;
         const long long src_off = mat + static_cast<long long>(ok ? src : 0) * row_bytes;
+        const long long all_bytes = static_cast<long long>(total) * row_bytes;
         for (int c = lane * 16; c < row_bytes; c += 32 * 16) {
+            // a checked build: both 16-byte vectors inside the [L][F] rows
+            if (!checked_range(src_off + c, 16, all_bytes, st, nullptr, kWhereBoundsLoad) ||
+                !checked_range(dst_off + c, 16, all_bytes, st, nullptr, kWhereBoundsStore))
+                break;
             uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
             if (ok) {
                 a = __ldg(reinterpret_cast<const uint4*>(in0 + src_off + c));
@@ -109,7 +115,10 @@ __global__ void __launch_bounds__(512) permute_cols_kernel(const T* in, T* out, 
                 } pack;
 #pragma unroll
                 for (int k = 0; k < E; ++k) pack.e[k] = idx[k] >= 0 ? row_s[idx[k]] : T(0);
-                reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * F)[c] = pack.u;
+                // a checked build: the output vector inside the [L][R][F] matrix
+                if (checked_range((static_cast<long long>(l) * R + r0 + r) * F + static_cast<long long>(c) * E, E,
+                                  static_cast<long long>(L) * R * F, st, nullptr, kWhereBoundsStore))
+                    reinterpret_cast<uint4*>(dst + static_cast<long long>(r) * F)[c] = pack.u;
             }
         }
     }

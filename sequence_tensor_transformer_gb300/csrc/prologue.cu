@@ -124,10 +124,15 @@ __global__ void __launch_bounds__(1024) prologue_rows(const __grid_constant__ Pr
     for (long long base = static_cast<long long>(blockIdx.x) * R; base < total;
          base += static_cast<long long>(gridDim.x) * R) {
         const long long gr = base + grp;
-        const bool active = gr < total;
         // no division for one group; a 32-bit one otherwise (G * M < 2^31)
-        const int g = active && p.G > 1 ? static_cast<int>(static_cast<uint32_t>(gr) / static_cast<uint32_t>(p.M)) : 0;
-        const long long row = active ? gr - static_cast<long long>(g) * p.M : 0;
+        const int g = gr < total && p.G > 1 ? static_cast<int>(static_cast<uint32_t>(gr) / static_cast<uint32_t>(p.M))
+                                            : 0;
+        const long long row = gr < total ? gr - static_cast<long long>(g) * p.M : 0;
+        // a checked build: the (group, row) and the group's source list
+        const bool active = gr < total &&
+                            checked(g < p.G && row < p.M && p.grp[g].src_begin >= 0 &&
+                                        p.grp[g].src_begin + p.grp[g].n_src <= kMaxSrc,
+                                    p.status, nullptr, kWhereBoundsTile, gr);
         const PrologueGroup& grpd = p.grp[g];
         const long long off = row * d;
         float h[VPT][E];
@@ -251,6 +256,12 @@ __global__ void __launch_bounds__(512) prologue_tma(const __grid_constant__ Prol
         locate(first + i * stride, g, row);
         const PrologueGroup& grp = p.grp[g];
         uint8_t* st = smem + static_cast<size_t>(s) * stage_bytes;
+        // a checked build: the (group, row), the group's sources and the
+        // stage; a failed check copies nothing, the row's wait gives up
+        if (!checked(g < p.G && row < p.M && grp.src_begin >= 0 && grp.src_begin + grp.n_src <= kMaxSrc &&
+                         grp.n_src <= L.max_src && s < L.S,
+                     p.status, &abort_flag, kWhereBoundsLoad, row))
+            return;
         mbar_arrive_expect_tx(&full[s], slot_bytes * static_cast<uint32_t>(grp.n_src + 1));
         const long long off = row * static_cast<long long>(slot_bytes);
         bulk_load(st, static_cast<const uint8_t*>(grp.x) + off, slot_bytes, &full[s]);

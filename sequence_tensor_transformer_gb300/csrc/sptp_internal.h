@@ -35,6 +35,14 @@ enum : int {
     kWhereFusedRows = 10,
     kWhereFusedGateUp = 11,
     kWherePermIndex = 12,
+    // bounds-checked builds (SPTP_BOUNDS_CHECK): what failed its check
+    kWhereBoundsTile = 20,     // a decoded tile or row index outside its range
+    kWhereBoundsCounter = 21,  // a readiness-counter index
+    kWhereBoundsRing = 22,     // a pending-ring slot, module or source shard
+    kWhereBoundsCluster = 23,  // the cluster shape or a CTA's rank in it
+    kWhereBoundsTma = 24,      // a TMA box origin (alignment or range)
+    kWhereBoundsStore = 25,    // a global store outside its buffer
+    kWhereBoundsLoad = 26,     // a global load or bulk copy outside its buffer
 };
 
 // Default limit of every bounded device-side wait (ns). A legitimate wait in

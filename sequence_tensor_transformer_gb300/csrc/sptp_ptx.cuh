@@ -124,6 +124,73 @@ __device__ __forceinline__ bool warp_flag_wait_geq(const int* flag, int target, 
     }
 }
 
+// ---------------------------------------------------------------- bounds-checked builds
+// Built with -DSPTP_BOUNDS_CHECK, the kernels check the indices and
+// addresses they compute -- decoded tiles, readiness counters, pending-ring
+// slots, the cluster shape, TMA box origins, global loads and stores --
+// against the buffers they address before using them.  A failed check
+// records SPTP_ERR_BOUNDS (-11), the place (kWhereBounds*) and the offending
+// value in the status words, raises the CTA's abort flag and skips the
+// access; the kernel then leaves through its bounded waits.  In the normal
+// build every check is the constant true and compiles to nothing.
+#ifdef SPTP_BOUNDS_CHECK
+constexpr bool kBoundsChecked = true;
+#else
+constexpr bool kBoundsChecked = false;
+#endif
+
+__device__ __forceinline__ void report_bounds(DeviceStatus* st, volatile int* abort_flag, int where, long long value) {
+    if (abort_flag != nullptr) *abort_flag = 1;
+    if (st != nullptr && atomicCAS(&st->code, 0, -11 /* SPTP_ERR_BOUNDS */) == 0) {
+        st->where = where;
+        st->block = blockIdx.x;
+        const long long lim = 0x7fffffffll;
+        st->info = static_cast<int>(value > lim ? lim : (value < -lim ? -lim : value));
+    }
+}
+
+// true if ok; in a checked build a false `ok` is recorded and false returned.
+__device__ __forceinline__ bool checked(bool ok, DeviceStatus* st, volatile int* abort_flag, int where,
+                                        long long value) {
+    if constexpr (kBoundsChecked) {
+        if (!ok) {
+            report_bounds(st, abort_flag, where, value);
+            return false;
+        }
+    }
+    return true;
+}
+
+// [off, off + n) within [0, limit) (elements or bytes)
+__device__ __forceinline__ bool checked_range(long long off, long long n, long long limit, DeviceStatus* st,
+                                              volatile int* abort_flag, int where) {
+    return checked(off >= 0 && off + n <= limit, st, abort_flag, where, off);
+}
+
+// 0 <= i < n
+__device__ __forceinline__ bool checked_index(long long i, long long n, DeviceStatus* st, volatile int* abort_flag,
+                                              int where) {
+    return checked(i >= 0 && i < n, st, abort_flag, where, i);
+}
+
+// A TMA box origin: the inner coordinate x aligned to `align` elements (16
+// bytes and more) and inside [0, extent_x); the row coordinate inside
+// [0, extent_rows) (a box may hang over the end and is zero-filled there).
+__device__ __forceinline__ bool checked_tma(int x, int align, int extent_x, long long row, long long extent_rows,
+                                            DeviceStatus* st, volatile int* abort_flag) {
+    if constexpr (kBoundsChecked) {
+        if (x < 0 || x % align != 0 || x >= extent_x) return checked(false, st, abort_flag, kWhereBoundsTma, x);
+        if (row < 0 || row >= extent_rows) return checked(false, st, abort_flag, kWhereBoundsTma, row);
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -23,7 +23,8 @@ def pytest_sessionfinish(session, exitstatus):
     if path:
         import helpers
         with open(path, "w") as f:
-            json.dump(helpers.OBSERVED, f, indent=1, sort_keys=True)
+            json.dump({k: {"max": v, "test": helpers.OBSERVED_AT.get(k)} for k, v in helpers.OBSERVED.items()}, f,
+                      indent=1, sort_keys=True)
 
 
 @pytest.fixture(scope="session")
