@@ -498,7 +498,7 @@ int sptp_ffn_forward_ex(const void* x, const void* partials, const void* gamma, 
     // 7: row-parallel down projection, one partial per shard
     void* outs[kMaxGroups];
     for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * act);
-    return down(sbuf, W2, M, d, F, P, dtype, outs, ws_status(workspace), band, di, s);
+    return down(sbuf, W2, M, d, F, P, dtype, outs, ws_status(workspace), down_raster_band(), di, s);
 }
 
 size_t dtp_ffn_stack_workspace_size(int M, int d, int F, int P, int L, int delta, sptp_dtype dtype) {
@@ -606,7 +606,7 @@ int dtp_ffn_stack_forward_ex(void* x_shards, const void* gamma, const void* W1g,
                          raster_band(), di, s)) != SPTP_OK)
             return rc;
         for (int p = 0; p < P; ++p) outs[p] = o(l, p);
-        if ((rc = down(sbuf, cptr(W2, woff), M, d, F, P, dtype, outs, ws_status(workspace), raster_band(),
+        if ((rc = down(sbuf, cptr(W2, woff), M, d, F, P, dtype, outs, ws_status(workspace), down_raster_band(),
                        di, s)) != SPTP_OK)
             return rc;
         (void)f;
@@ -694,7 +694,7 @@ int sptp_down_proj(const void* s_in, const void* W2, int M, int d, int F, int P,
     if ((rc = reset_status(workspace, s)) != SPTP_OK) return rc;
     void* outs[kMaxGroups];
     for (int g = 0; g < P; ++g) outs[g] = mptr(out, static_cast<size_t>(g) * M * d * es);
-    return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), raster_band(), di, s);
+    return down(s_in, W2, M, d, F, P, dtype, outs, ws_status(workspace), down_raster_band(), di, s);
 }
 
 size_t sptp_attn_qkv_workspace_size(int M, int d, int N, int P, int chunks, sptp_dtype dtype) {

@@ -20,6 +20,14 @@ constexpr int kBandRows = 4096;
 
 int raster_band() { return kBandRows / kBM; }
 
+// Raster band of the down GEMM (rows).  A build option (-DSPTP_DOWN_BAND_ROWS)
+// for measuring the effect of the band on the down GEMM's DRAM traffic.
+#ifndef SPTP_DOWN_BAND_ROWS
+#define SPTP_DOWN_BAND_ROWS 4096
+#endif
+
+int down_raster_band() { return SPTP_DOWN_BAND_ROWS / kBM; }
+
 // Gate/up + SwiGLU for P groups: s_g = silu(A_g W1g[F_g]^T) * (A_g W1u[F_g]^T).
 int gateup(const void* const* A, const void* W1g, const void* W1u, int M, int d, int F, int P, int dtype,
            void* s_out, DeviceStatus* st, int band, const DevInfo& di, cudaStream_t s) {

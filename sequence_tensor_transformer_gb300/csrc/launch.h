@@ -26,8 +26,9 @@ inline const char* cptr(const void* base, size_t off_bytes) { return static_cast
 inline char* mptr(void* base, size_t off_bytes) { return static_cast<char*>(base) + off_bytes; }
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? SPTP_OK : SPTP_ERR_CUDA; }
 
-// m-tiles (128 rows) per raster band
+// m-tiles (128 rows) per raster band, of the gate/up and of the down GEMM
 int raster_band();
+int down_raster_band();
 
 // Gate/up + SwiGLU for P groups: s_g = silu(A_g W1g[F_g]^T) * (A_g W1u[F_g]^T);
 // s_out [P][M][F/P].
