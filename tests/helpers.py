@@ -21,13 +21,26 @@ from sequence_tensor_transformer_gb300 import synth
 TOL = {"bf16": 2e-2, "fp32": 1e-5}
 
 # Regression bounds, about twice the largest rel. max error observed on
-# GB300 in each family of tests; a change that makes the arithmetic 2-3x
-# less accurate fails here long before it reaches the acceptance bar.
+# GB300 in each family of tests (in brackets, with the test that saw it); a
+# change that makes the arithmetic 2-3x less accurate fails here long before
+# it reaches the acceptance bar.
 REGRESSION = {
-    "bf16": 2e-2,       # bf16 boundary, Delayed TP, attention
-    "bf16_step": 2e-2,  # single GEMM launches
-    "e4m3": 2e-2,       # fp8 boundary and GEMMs
-    "fp32": 1e-5,
+    # bf16 boundary, Delayed TP, attention [7.6e-3, the Delayed-TP stack
+    # workload, per-module launches]
+    "bf16": 1.5e-2,
+    # single bf16 GEMM launches on N(0, 1) operands [3.1e-3, down projection]
+    "bf16_step": 7e-3,
+    # fp8 boundary and GEMMs [1.95e-2, P = 8 with F/P = 256]: the oracle takes
+    # the bf16 roundings of y and s in float64, the kernels in fp32, so a
+    # value next to a rounding boundary can get a neighbouring E4M3 code on
+    # the two sides; one such code moves one term of a K-term down-projection
+    # sum by up to an eighth of it, which at K = 256 reaches 2e-2 of the
+    # output range.  A CPU restatement of the kernels' fp32 steps gives the
+    # same 1.95e-2 against the oracle, so this is the oracle's precision, not
+    # the kernels'; the bound stays at the acceptance bar.
+    "e4m3": 2e-2,
+    # fp32 CUDA-core path [1.6e-6, gate/up + SwiGLU]
+    "fp32": 4e-6,
 }
 
 # largest error seen per family in this session, and the test that saw it
