@@ -1,7 +1,7 @@
 """Oracle for the fp8 (E4M3) variant of the SP-TP FFN boundary.
 
-TEST INFRASTRUCTURE ONLY: a plain float64 CPU statement of what the fp8 path
-of the CUDA library computes.  Only the tests, the package smoke check and the
+TEST INFRASTRUCTURE ONLY: a plain CPU statement of what the fp8 path of the
+CUDA library computes (float64, with fp32 where a value decides a code).  Only the tests, the package smoke check and the
 benchmark's CPU legs may import it; the product path never calls it.
 
 Source (web page; title and section): "[Feature] Async Tensor Parallelism for
@@ -26,6 +26,15 @@ design notes:
   real TP rank quantises its local shard.
 * A GEMM of quantised operands is sum_k qa qb times 2^(e_a + e_b); gate and
   up values are dequantised before SwiGLU.
+* Where a value decides a code -- y and s, whose bf16 roundings are then
+  quantised to E4M3 -- this oracle computes it in the precision the kernels
+  use, fp32 (the sums of partials, the mean square and the norm of y; the
+  gate/up accumulations, SwiGLU and the down accumulation), so that both
+  sides take each quantisation decision in the same precision.  A float64
+  value next to a rounding boundary could otherwise fall on the other side
+  of it, and one E4M3 code of s moves a term of a K-long down-projection sum
+  by up to an eighth.  The fp32 sums run in numpy's order, not the kernels';
+  the products of E4M3 values are exact in fp32.
 
 Parity status: round_bf16 and round_e4m3 are pinned against PyTorch's casts;
 e4m3_row_exponent by closed forms and minimality; the composition by a
@@ -36,7 +45,6 @@ from __future__ import annotations
 
 import numpy as np
 
-from .sptp_oracle import reduce_partials, rms_norm, silu
 
 E4M3_MAX = 448.0
 MIN_EXPONENT = -126
@@ -126,30 +134,71 @@ def quantize_ffn_weights(W1g, W1u, W2, P: int):
     return qg, eg, qu, eu, q2.reshape(d, F), e2
 
 
+def _f32(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float32)
+
+
+def _gemm_f32(qa, ea, qb, eb) -> np.ndarray:
+    """(sum_k qa[r][k] qb[c][k]) * 2^ea[r] * 2^eb[c] in fp32: the products of
+    E4M3 values are exact, the sum is an fp32 sum, and each scale is a power
+    of two applied as an fp32 multiplication (row scale first).  Each row is
+    its own matrix-vector product, so a row's result does not depend on which
+    other rows are evaluated with it (row samples equal the full result)."""
+    qa32, qb32 = _f32(qa), _f32(qb)
+    acc = np.zeros((qa32.shape[0], qb32.shape[0]), dtype=np.float32)
+    for r in range(qa32.shape[0]):
+        acc[r] = qb32 @ qa32[r]
+    return (acc * _f32(np.ldexp(1.0, ea))[:, None]) * _f32(np.ldexp(1.0, eb))[None, :]
+
+
+def _silu_f32(a: np.ndarray) -> np.ndarray:
+    """silu(a) = a / (1 + e^-a) in fp32 (e^-a overflowing to inf gives -0)."""
+    with np.errstate(over="ignore"):
+        return a / (np.float32(1.0) + np.exp(-a))
+
+
 def shard_ffn_fp8(y, qw, P: int, p: int, return_intermediates: bool = False):
     """Shard p's fp8 gate/up GEMM, SwiGLU and fp8 down GEMM on bf16 rows y
-    [R][d]; qw = quantize_ffn_weights(...).  Returns the partial [R][d]
-    (float64, before any output rounding)."""
+    [R][d]; qw = quantize_ffn_weights(...).  The GEMMs accumulate in fp32 and
+    SwiGLU runs in fp32, so that s -- whose bf16 rounding decides the E4M3
+    codes of the down projection's input -- is computed in the kernels'
+    precision.  Returns the partial [R][d] (float64 holding the fp32 values,
+    before the output's bf16 rounding)."""
     qg, eg, qu, eu, q2, e2 = qw
     F = qg.shape[0]
     f = F // P
     n = slice(p * f, (p + 1) * f)
     qy, ey = quantize_rows_e4m3(y)
-    sy = np.ldexp(1.0, ey)[:, None]
-    a = (qy @ qg[n].T) * sy * np.ldexp(1.0, eg[n])[None, :]
-    b = (qy @ qu[n].T) * sy * np.ldexp(1.0, eu[n])[None, :]
-    s = round_bf16(silu(a) * b)
+    a = _gemm_f32(qy, ey, qg[n], eg[n])
+    b = _gemm_f32(qy, ey, qu[n], eu[n])
+    s = round_bf16((_silu_f32(a) * b).astype(np.float64))
     qs, es = quantize_rows_e4m3(s)
-    out = (qs @ q2[:, n].T) * np.ldexp(1.0, es)[:, None] * np.ldexp(1.0, e2[:, p])[None, :]
+    out = _gemm_f32(qs, es, q2[:, n], e2[:, p]).astype(np.float64)
     if return_intermediates:
-        return out, dict(qy=qy, ey=ey, a=a, b=b, s=s, qs=qs, es=es)
+        return out, dict(qy=qy, ey=ey, a=a.astype(np.float64), b=b.astype(np.float64), s=s, qs=qs, es=es)
     return out
+
+
+def boundary_rows_fp32(x, partials, gamma, eps):
+    """h = x + (partials[0] + partials[1] + ...) and the bf16 activation
+    y = bf16((h * gamma) * 1 / sqrt(mean(h^2) + eps)), in fp32 (the partial sum
+    and the residual add, the mean square, the norm), as the kernels compute
+    the y that the gate/up linear quantises.  Returns (h, y) as float64."""
+    r = np.zeros(np.shape(x), dtype=np.float32)
+    for q in range(partials.shape[0]):
+        r = r + _f32(partials[q])
+    h = _f32(x) + r
+    ms = np.sum(h * h, axis=-1, dtype=np.float32) / np.float32(h.shape[-1])
+    inv = np.float32(1.0) / np.sqrt(ms + np.float32(eps))
+    y = round_bf16(((h * _f32(gamma)) * inv[:, None]).astype(np.float64))
+    return h.astype(np.float64), y
 
 
 def sptp_ffn_forward_fp8(x, partials, gamma, W1g, W1u, W2, P: int, chunks: int, eps: float, rows=None):
     """The SP-TP FFN boundary with fp8 linear layers: per chunk the P partials
-    are summed, the residual added and the sum RMS-normalised; y is the bf16
-    activation; every shard runs shard_ffn_fp8 on it.  Arguments and return
+    are summed, the residual added and the sum RMS-normalised (in fp32,
+    boundary_rows_fp32); y is the bf16 activation; every shard runs
+    shard_ffn_fp8 on it.  Arguments and return
     value as in the float64 boundary: (out [P, R, d], h [R, d])."""
     M, d = x.shape
     F = W1g.shape[0]
@@ -165,8 +214,7 @@ def sptp_ffn_forward_fp8(x, partials, gamma, W1g, W1u, W2, P: int, chunks: int, 
         if len(pos) == 0:
             continue
         r_idx = sel[pos]
-        h = x[r_idx] + reduce_partials(partials[:, r_idx, :])
-        y = round_bf16(rms_norm(h, gamma, eps))
+        h, y = boundary_rows_fp32(x[r_idx], partials[:, r_idx, :], gamma, eps)
         h_out[pos] = h
         for p in range(P):
             out[p, pos] = shard_ffn_fp8(y, qw, P, p)
