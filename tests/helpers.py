@@ -30,15 +30,12 @@ REGRESSION = {
     "bf16": 1.5e-2,
     # single bf16 GEMM launches on N(0, 1) operands [3.1e-3, down projection]
     "bf16_step": 7e-3,
-    # fp8 boundary and GEMMs [1.95e-2, P = 8 with F/P = 256]: the oracle takes
-    # the bf16 roundings of y and s in float64, the kernels in fp32, so a
-    # value next to a rounding boundary can get a neighbouring E4M3 code on
-    # the two sides; one such code moves one term of a K-term down-projection
-    # sum by up to an eighth of it, which at K = 256 reaches 2e-2 of the
-    # output range.  A CPU restatement of the kernels' fp32 steps gives the
-    # same 1.95e-2 against the oracle, so this is the oracle's precision, not
-    # the kernels'; the bound stays at the acceptance bar.
-    "e4m3": 2e-2,
+    # fp8 boundary and GEMMs [8.7e-3, P = 8 with F/P = 256]: both sides take
+    # every quantisation decision in fp32, but in different summation orders
+    # and with the kernels' fast exp and divide, so a rare value next to a
+    # rounding boundary still gets a neighbouring E4M3 code; one such code of
+    # s moves a term of the K = 256 down-projection sum by up to an eighth
+    "e4m3": 1.75e-2,
     # fp32 CUDA-core path [1.6e-6, gate/up + SwiGLU]
     "fp32": 4e-6,
 }
