@@ -35,6 +35,7 @@ enum : int {
     kWhereFusedRows = 10,
     kWhereFusedGateUp = 11,
     kWherePermIndex = 12,
+    kWherePermStage = 13,
     // bounds-checked builds (SPTP_BOUNDS_CHECK): what failed its check
     kWhereBoundsTile = 20,     // a decoded tile or row index outside its range
     kWhereBoundsCounter = 21,  // a readiness-counter index

@@ -158,8 +158,9 @@ def test_fp8_boundary_checked(M, d, F, P, C):
         assert rel_err(got[p], ref[p]) <= TOL["bf16"], p
 
 
-def test_permutation_checked():
-    L, d, F = 2, 136, 200
+@pytest.mark.parametrize("L,d,F", [(2, 136, 200), (3, 1024, 3072), (1, 8, 24576)])
+def test_permutation_checked(L, d, F):
+    """The pipelined launch (the first two) and the two-launch fallback."""
     rng = np.random.default_rng(3)
     W1g, W1u = synth._cast(rng.standard_normal((L, F, d)), "bf16"), synth._cast(rng.standard_normal((L, F, d)), "bf16")
     W2 = synth._cast(rng.standard_normal((L, d, F)), "bf16")

@@ -35,8 +35,13 @@ def _perms(L, F, seed):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-@pytest.mark.parametrize("L,d,F", [(1, 8, 8), (2, 136, 200), (4, 1024, 3072), (1, 4096, 14336)])
+@pytest.mark.parametrize("L,d,F", [(1, 8, 8), (3, 8, 24), (2, 136, 200), (4, 1024, 3072), (2, 64, 6144),
+                                   (1, 6144, 8), (1, 4096, 14336), (1, 16, 24576)])
 def test_permutation_kernel_is_exact_indexing(dtype, L, d, F):
+    """Both launch structures: the one-launch bulk-copy pipeline (a W1 row of
+    each matrix and a W2 row fit its 32 KiB stage: one or many rows per unit)
+    and the two-launch fallback for wider rows (F = 24576; in fp32 also
+    d = 6144 and F = 14336)."""
     rng = np.random.default_rng(L * d + F)
     W1g = synth._cast(rng.standard_normal((L, F, d)), dtype)
     W1u = synth._cast(rng.standard_normal((L, F, d)), dtype)
@@ -54,9 +59,10 @@ def test_permutation_kernel_is_exact_indexing(dtype, L, d, F):
         assert np.array_equal(view(outs[2])[l], W2[l][:, perm[l]])
 
 
-def test_out_of_range_index_is_reported_and_zero_filled():
-    L, d, F = 1, 64, 32
-    rng = np.random.default_rng(0)
+@pytest.mark.parametrize("d,F", [(64, 32), (8, 24576)])
+def test_out_of_range_index_is_reported_and_zero_filled(d, F):
+    """(64, 32) runs the pipelined launch, (8, 24576) the two-launch fallback."""
+    L = 1
     W = [torch.randn((L, F, d), device="cuda:0").to(torch.bfloat16) for _ in range(2)]
     W2 = torch.randn((L, d, F), device="cuda:0").to(torch.bfloat16)
     perm = np.arange(F, dtype=np.int32)[None].copy()
@@ -65,9 +71,12 @@ def test_out_of_range_index_is_reported_and_zero_filled():
     ws = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device="cuda:0")
     g, u, w2 = st.sptp_permute_ffn_neurons(W[0], W[1], W2, torch.from_numpy(perm).cuda(), workspace=ws)
     assert st.sptp_read_device_status(ws) == -2
-    assert torch.count_nonzero(g[0, 3]) == 0 and torch.count_nonzero(g[0, 7]) == 0
-    assert torch.count_nonzero(w2[0][:, 3]) == 0
-    assert torch.equal(g[0, 4], W[0][0, 4]) and torch.equal(w2[0][:, 4], W2[0][:, 4])
+    for t in (g, u):
+        assert torch.count_nonzero(t[0, 3]) == 0 and torch.count_nonzero(t[0, 7]) == 0
+    assert torch.count_nonzero(w2[0][:, 3]) == 0 and torch.count_nonzero(w2[0][:, 7]) == 0
+    keep = [i for i in range(F) if i not in (3, 7)]
+    assert torch.equal(g[0, keep], W[0][0, keep]) and torch.equal(u[0, keep], W[1][0, keep])
+    assert torch.equal(w2[0][:, keep], W2[0][:, keep])
 
 
 def run_permuted_dtp(cfg, perms, flush, rows=None, variant="auto"):
