@@ -217,32 +217,6 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
         : "memory");
 }
 
-// Bulk (non-tensor) copy of `bytes` (multiple of 16, 16-byte aligned ends)
-// from this CTA's shared memory to global memory, in the issuing thread's
-// current bulk async-group.
-__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
-                 "r"(smem_u32(smem_src)), "r"(bytes)
-                 : "memory");
-}
-
-// Closes the issuing thread's current bulk async-group.
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Waits until at most N of the issuing thread's bulk async-groups still read
-// their shared-memory sources (their global writes may still be in flight).
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Waits until at most N of the issuing thread's bulk async-groups are
-// incomplete.
-template <int N>
-__device__ __forceinline__ void bulk_wait() {
-    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Orders this thread's earlier generic-proxy accesses before later
 // async-proxy (TMA) accesses of shared memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
