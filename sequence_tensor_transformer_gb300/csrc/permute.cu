@@ -191,14 +191,14 @@ __device__ __forceinline__ Unit unit_at(const Params& p, int u) {
     return x;
 }
 
-// Warp 0: arms stage s and issues unit u's loads into it.
 // Lane r's source index for kind-A unit x (row first + r), or -1.
 __device__ __forceinline__ int unit_index(const Params& p, const Unit& x, int lane) {
     return x.a && lane < x.n ? p.perm[static_cast<long long>(x.l) * p.F + x.first + lane] : -1;
 }
 
-// idx: this lane's unit_index, loaded ahead so that its latency overlaps the
-// previous units' issue.
+// Warp 0: arms stage s and issues unit x's loads into it.  idx: this lane's
+// unit_index, loaded ahead so that its latency overlaps the previous units'
+// issue.
 __device__ __forceinline__ void issue_loads(const Params& p, const Unit& x, int idx, uint8_t* stage, Bars* bars,
                                             int s, int lane, volatile int* abort_flag) {
     const long long row_bytes = static_cast<long long>(p.d) * p.es;
