@@ -45,13 +45,27 @@ def parse():
                     help="seconds of back-to-back boundary calls for the power-capped (sustained) figure")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other workloads' figures (the 'configs' key)")
-    ap.add_argument("--workload", choices=["boundary", "dtp", "attn", "permute", "fp8", "msweep", "qwen2"],
+    ap.add_argument("--workload", choices=["boundary", "tiny", "dtp", "attn", "permute", "fp8", "msweep", "qwen2"],
                     default="boundary",
                     help="boundary: the SP-TP FFN boundary (the default, headline line); the others measure "
-                         "the Delayed-TP stack, the attention-side boundary, the neuron permutation, the "
-                         "boundary with E4M3 linear layers, the M sweep (d=4096, F=16384, P=8) and the "
-                         "Qwen2-7B-shaped boundary")
-    return ap.parse_args()
+                         "the tiny fp32 boundary, the Delayed-TP stack, the attention-side boundary, the neuron "
+                         "permutation, the boundary with E4M3 linear layers, the M sweep (d=4096, F=16384, P=8) "
+                         "and the Qwen2-7B-shaped boundary")
+    ap.add_argument("--config", type=int, choices=range(len(CONFIG_WORKLOADS)),
+                    help="a workload by its index in the list of workloads: " +
+                         ", ".join(f"{i} {w}" for i, w in enumerate(CONFIG_WORKLOADS)))
+    args = ap.parse_args()
+    if args.config is not None:
+        args.workload = CONFIG_WORKLOADS[args.config]
+    return args
+
+
+# The five workloads in order: the tiny fp32 boundary (M=64, d=128, F=512, P=2,
+# C=4), the bf16 boundary (M=8192, d=4096, F=14336, P=2, C=8), the Qwen2-7B
+# shape (M=16384, d=3584, F=18944, P=4, C=16), the M sweep (M=4096..65536,
+# d=4096, F=16384, P=8, C=8) and the Delayed-TP stack (L=4, M=4096, d=1024,
+# F=3072, P=2, delta=1).
+CONFIG_WORKLOADS = ("tiny", "boundary", "qwen2", "msweep", "dtp")
 
 
 def workload():
@@ -890,6 +904,53 @@ def run_other(args):
                               "peak_kind": r["peak_kind"]})
     elif args.workload == "fp8":
         line.update(_fp8_line(args, synth.BOUNDARY_D4096, to_dev, dev, stream, pk))
+    elif args.workload == "tiny":
+        # the fp32 workload: 64 token rows, launch-bound; CUDA-core GEMMs (fp32 arithmetic)
+        cfg = synth.TINY_FP32
+        inp = synth.boundary_inputs(cfg)
+        T = {k: torch.from_numpy(np.ascontiguousarray(v)).to(dev) for k, v in inp.items()}
+        out = torch.empty((cfg.P, cfg.M, cfg.d), dtype=torch.float32, device=dev)
+        h = torch.empty_like(T["x"])
+        ws = torch.empty(st.sptp_ffn_workspace_size(cfg.M, cfg.d, cfg.F, cfg.P, cfg.chunks, st.SPTP_FP32),
+                         dtype=torch.uint8, device=dev)
+
+        def fn():
+            st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], cfg.P, cfg.chunks,
+                                cfg.eps, out=out, resid_out=h, workspace=ws)
+        ms, n = time_calls(fn, stream, seconds=0.3)
+        status = st.sptp_read_device_status(ws)
+        fl = 6.0 * cfg.M * cfg.d * cfg.F
+        # back-to-back calls from Python are bound by the host; the same calls
+        # replayed from a CUDA graph (100 calls per graph) give the device time
+        graph = None
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                fn()
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(100):
+                    fn()
+            ms_g, n_g = time_calls(g.replay, stream, seconds=0.3)
+            graph = {"ms_per_call": ms_g / 100, "tflops": fl / (ms_g / 100 * 1e-3) / 1e12,
+                     "tokens_per_s": cfg.M / (ms_g / 100 * 1e-3), "calls": 100 * n_g,
+                     "device_status": st.sptp_read_device_status(ws)}
+        except Exception as e:  # capture is a measurement aid, not part of the library's contract
+            graph = {"unavailable": str(e).splitlines()[0][:200]}
+        csec = oracle_rate(cfg, cfg.M)
+        cpu = {"value": fl / csec / 1e12, "unit": "TFLOP/s", "tokens_per_s": cfg.M / csec, "cores": cores(),
+               "kind": "oracle", "sample": f"all {cfg.M} token rows of {cfg.name}, float64 numpy oracle, "
+                                           f"{csec:.4f} s"}
+        line.update(metric="SP-TP FFN forward TFLOP/s & tokens/s: " + cfg.name, value=fl / (ms * 1e-3) / 1e12,
+                    unit="TFLOP/s", ms_per_step=ms, dtype="fp32", tokens_per_s=cfg.M / (ms * 1e-3), calls=n,
+                    device_status=status, cpu_baseline=cpu, graph_replay=graph,
+                    config={"workload": cfg.name, "l2": "inputs fit in L2 (0.8 MB), back-to-back calls"},
+                    roofline={"bound": "latency", "achieved_us_per_call": ms * 1e3,
+                              "note": "25 MFLOP per call in three launches: launch and latency bound, so no "
+                                      "throughput roofline applies; parity is tests/test_gpu_parity.py's fp32 case"})
     elif args.workload in ("msweep", "qwen2"):
         if args.workload == "msweep":
             per = leg_msweep(st, synth, dev, stream, pk, seconds=1.0)
