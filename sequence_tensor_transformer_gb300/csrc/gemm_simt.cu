@@ -2,15 +2,17 @@
 // cannot meet a 1e-5 relative error bound).  Same two shapes as the tcgen05
 // path: gate/up with a SwiGLU epilogue and the per-shard down projection,
 // C_g[m][n] = sum_k A_g[m][k] * B_g[n][k] with both operands K-contiguous.
-// 64 x 64 tile per CTA, 16-deep K slices staged in shared memory, 4 x 4
-// outputs per thread, fp32 FMA in ascending k.
+// 64 x 64 tile per CTA, 32-deep K slices staged in shared memory (the next
+// slice's loads in flight in registers while the current one is multiplied),
+// 4 x 4 outputs per thread, fp32 FMA in ascending k.
 #include "sptp_internal.h"
 
 namespace sptp {
 
 namespace {
 
-constexpr int TM = 64, TN = 64, TK = 16;
+constexpr int TM = 64, TN = 64, TK = 32;
+constexpr int kLoads = TM * TK / 256;  // elements of each operand a thread stages per slice
 
 template <Epi EPI>
 __global__ void __launch_bounds__(256) simt_gemm_nt(const __grid_constant__ SimtGemmParams p) {
@@ -25,18 +27,32 @@ __global__ void __launch_bounds__(256) simt_gemm_nt(const __grid_constant__ Simt
     const float* B0 = p.B0[g];
     const float* B1 = p.B1[g];
     float acc0[4][4] = {}, acc1[4][4] = {};
-    for (int k0 = 0; k0 < p.K; k0 += TK) {
+    // slice k0 of both operands into registers (zero past M, N or K)
+    float ra[kLoads], rb0[kLoads], rb1[SWI ? kLoads : 1];
+    auto fetch = [&](int k0) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kLoads; ++i) {
             const int idx = threadIdx.x + i * 256;
             const int r = idx / TK, kk = idx % TK;
             const int k = k0 + kk;
             const int am = m0 + r, bn = n0 + r;
-            As[kk][r] = (am < p.M && k < p.K) ? A[am * p.lda + k] : 0.f;
-            Bs0[kk][r] = (bn < p.N && k < p.K) ? B0[bn * p.ldb + k] : 0.f;
-            if (SWI) Bs1[kk][r] = (bn < p.N && k < p.K) ? B1[bn * p.ldb + k] : 0.f;
+            ra[i] = (am < p.M && k < p.K) ? A[static_cast<long long>(am) * p.lda + k] : 0.f;
+            rb0[i] = (bn < p.N && k < p.K) ? B0[static_cast<long long>(bn) * p.ldb + k] : 0.f;
+            if (SWI) rb1[i] = (bn < p.N && k < p.K) ? B1[static_cast<long long>(bn) * p.ldb + k] : 0.f;
+        }
+    };
+    fetch(0);
+    for (int k0 = 0; k0 < p.K; k0 += TK) {
+#pragma unroll
+        for (int i = 0; i < kLoads; ++i) {
+            const int idx = threadIdx.x + i * 256;
+            const int r = idx / TK, kk = idx % TK;
+            As[kk][r] = ra[i];
+            Bs0[kk][r] = rb0[i];
+            if (SWI) Bs1[kk][r] = rb1[i];
         }
         __syncthreads();
+        if (k0 + TK < p.K) fetch(k0 + TK);  // in flight during this slice's FMAs
 #pragma unroll
         for (int kk = 0; kk < TK; ++kk) {
             float a[4], b0[4], b1[4];
