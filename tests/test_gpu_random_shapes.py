@@ -133,3 +133,45 @@ def test_random_attention_boundary(seed, variant):
     errs = {p: rel_err(got[p], ref[p]) for p in range(P)}
     errs["h"] = rel_err(host_f64(h), href)
     check_errors(errs, "bf16")
+
+
+def perm_shapes(seed, n):
+    """n (L, d, F) shapes with d and F multiples of 8: rows that fit the
+    pipelined launch's stage and wider ones that take the two-launch path."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        L = int(rng.integers(1, 4))
+        d = 8 * int(rng.integers(1, 257))
+        F = 8 * int(rng.integers(1, 1537))
+        if L * d * F <= (1 << 24):  # at most 16 M elements per matrix
+            out.append((L, d, F))
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("shape", perm_shapes(211, 8))
+def test_random_permutation(shape, dtype):
+    """sptp_permute_ffn_neurons moves bytes only: its outputs equal plain
+    indexing exactly, whichever launch structure the shape takes."""
+    L, d, F = shape
+    rng = np.random.default_rng(L * 100003 + d * 31 + F)
+    W1g = synth._cast(rng.standard_normal((L, F, d)), dtype)
+    W1u = synth._cast(rng.standard_normal((L, F, d)), dtype)
+    W2 = synth._cast(rng.standard_normal((L, d, F)), dtype)
+    perm = np.stack([rng.permutation(F) for _ in range(L)]).astype(np.int32)
+    hdr = nan_workspace(st.SPTP_WS_HEADER_BYTES)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    outs = [torch.full((L, F, d), float("nan"), dtype=tdt, device="cuda:0") for _ in range(2)]
+    outs.append(torch.full((L, d, F), float("nan"), dtype=tdt, device="cuda:0"))
+    st.lib().sptp_permute_ffn_neurons(
+        *[t.data_ptr() for t in (dev_tensor(W1g, dtype), dev_tensor(W1u, dtype), dev_tensor(W2, dtype))],
+        torch.from_numpy(perm).cuda().data_ptr(), L, d, F, st.SPTP_BF16 if dtype == "bf16" else st.SPTP_FP32,
+        *[t.data_ptr() for t in outs], hdr.data_ptr(), hdr.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st.sptp_read_device_status(hdr) == 0
+    view = (lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)) if dtype == "bf16" else \
+        (lambda t: t.cpu().numpy())
+    for l in range(L):
+        assert np.array_equal(view(outs[0])[l], W1g[l][perm[l]])
+        assert np.array_equal(view(outs[1])[l], W1u[l][perm[l]])
+        assert np.array_equal(view(outs[2])[l], W2[l][:, perm[l]])
