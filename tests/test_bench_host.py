@@ -63,3 +63,20 @@ def test_clock_summary(bench):
     assert cs.summary()["reasons"] == ["hw_slowdown", "sw_power_cap"]
     empty = bench.ClockSampler(0)
     assert empty.summary() is None
+
+
+def test_config_index_selects_the_workload(bench, monkeypatch):
+    """--config N names the five workloads in their listed order; without it
+    the boundary (the headline line) runs."""
+    import sys
+    expect = ["tiny", "boundary", "qwen2", "msweep", "dtp"]
+    assert list(bench.CONFIG_WORKLOADS) == expect
+    for i, w in enumerate(expect):
+        monkeypatch.setattr(sys, "argv", ["bench.py", "--config", str(i)])
+        assert bench.parse().workload == w
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert a.workload == "boundary" and a.config is None
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--config", "5"])
+    with pytest.raises(SystemExit):
+        bench.parse()
