@@ -682,12 +682,15 @@ def leg_boundary(st, cfg, T, dev, stream, pk, variant="auto", seconds=0.3, parit
             "parity": parity}
 
 
-def leg_msweep(st, synth, dev, stream, pk, seconds=0.3):
-    """The M sweep at d=4096, F=16384, P=8, chunks=8, every M."""
+def leg_msweep(st, synth, dev, stream, pk, seconds=0.3, pause=0.0):
+    """The M sweep at d=4096, F=16384, P=8, chunks=8, every M (each after
+    `pause` seconds idle)."""
     import torch
     res = []
     for cfg in synth.M_SWEEP:
         T = boundary_tensors(cfg, dev)
+        torch.cuda.synchronize()
+        time.sleep(pause)
         res.append(leg_boundary(st, cfg, T, dev, stream, pk, seconds=seconds,
                                 parity="tests/test_gpu_parity.py::test_m_sweep_full_size_sampled_rows "
                                        "(sampled rows against the oracle, every variant, M = 4096/16384/65536)"))
@@ -807,19 +810,25 @@ def configs_leg(args, st, synth, dev, stream, pk):
     here the device status and finite outputs are checked."""
     import torch
     t0 = time.perf_counter()
-    res = {}
+    res = {"note": "each leg after 1 s idle, so that its short region runs at the clock the burst peak it is "
+                   "compared with was measured at, not at the power-capped clock the legs before leave"}
+    idle = lambda: (torch.cuda.synchronize(), time.sleep(1.0))
     cfg = synth.QWEN2_7B_SHAPE
     T = boundary_tensors(cfg, dev)
+    idle()
     res["qwen2_7b_shape"] = leg_boundary(
         st, cfg, T, dev, stream, pk, parity="tests/test_gpu_parity.py::"
         "test_boundary_qwen2_7b_shape_full_size_sampled_rows (sampled rows against the oracle, every variant)")
     del T
     torch.cuda.empty_cache()
-    res["m_sweep"] = leg_msweep(st, synth, dev, stream, pk)
+    res["m_sweep"] = leg_msweep(st, synth, dev, stream, pk, pause=1.0)
+    idle()
     res["dtp_stack"] = leg_dtp(st, synth, dev, stream, pk)
     torch.cuda.empty_cache()
+    idle()
     res["attention_boundary"] = leg_attn(st, synth, dev, stream, pk)
     torch.cuda.empty_cache()
+    idle()
     res["e4m3_boundary"] = leg_fp8(st, synth, dev, stream, pk)
     torch.cuda.empty_cache()
     res["seconds"] = time.perf_counter() - t0
