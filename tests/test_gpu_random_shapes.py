@@ -65,6 +65,42 @@ def test_random_boundary_bf16(shape, variant):
     check_boundary(cfg, out, h, ref, href, "bf16")
 
 
+def fp32_shapes(seed, n):
+    """Smaller boundary shapes for the fp32 CUDA-core path, with K (d and
+    F/P) off its 32-deep slice and M off its 64-row tile."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        P = int(rng.integers(1, 5))
+        C = P * int(rng.integers(1, 3))
+        M = C * int(rng.integers(1, 300 // C + 1))
+        d = 8 * int(rng.integers(1, 65))
+        F = P * 8 * int(rng.integers(1, 49))
+        out.append((M, d, F, P, C))
+    return out
+
+
+@pytest.mark.parametrize("shape", fp32_shapes(303, 6))
+def test_random_boundary_fp32(shape):
+    M, d, F, P, C = shape
+    cfg = synth.BoundaryConfig(f"r32_{M}_{d}_{F}_{P}_{C}", M, d, F, P, C, "fp32", False, seed=M + d)
+    inp = synth.boundary_inputs(cfg)
+    T = {k: dev_tensor(v, "fp32") for k, v in inp.items()}
+    ws = nan_workspace(st.sptp_ffn_workspace_size(M, d, F, P, C, st.SPTP_FP32))
+    out, h = nan_tensor((P, M, d), torch.float32), nan_tensor((M, d), torch.float32)
+    st.sptp_ffn_forward(T["x"], T["partials"], T["gamma"], T["W1g"], T["W1u"], T["W2"], P, C, cfg.eps, out=out,
+                        resid_out=h, workspace=ws)
+    assert st.sptp_read_device_status(ws) == 0
+    assert_no_nan(out, h)
+    f64 = {k: to_f64(v, "fp32") for k, v in inp.items()}
+    ref, href = oracle.sptp_ffn_forward(f64["x"], f64["partials"], f64["gamma"], f64["W1g"], f64["W1u"], f64["W2"],
+                                        P, C, cfg.eps)
+    got = host_f64(out)
+    errs = {p: rel_err(got[p], ref[p]) for p in range(P)}
+    errs["h"] = rel_err(host_f64(h), href)
+    check_errors(errs, "fp32", "fp32")
+
+
 @pytest.mark.parametrize("shape", shapes(202, 8, mult=16))
 def test_random_boundary_fp8(shape):
     M, d, F, P, C = shape
