@@ -1037,9 +1037,18 @@ def _fp8_line(args, cfg, to_dev, dev, stream, pk):
     out = torch.empty((P, M, d), dtype=torch.bfloat16, device=dev)
     h = torch.empty_like(T["x"])
     ws = torch.empty(st.sptp_ffn_fp8_workspace_size(M, d, F, P, cfg.chunks), dtype=torch.uint8, device=dev)
-    ms = timed(lambda: st.sptp_ffn_forward_fp8(T["x"], T["partials"], T["gamma"], qw, P, cfg.chunks, cfg.eps,
-                                               out=out, resid_out=h, workspace=ws), args.steps, args.warmup, stream)
+    def step():
+        st.sptp_ffn_forward_fp8(T["x"], T["partials"], T["gamma"], qw, P, cfg.chunks, cfg.eps, out=out, resid_out=h,
+                                workspace=ws)
+    ms = timed(step, args.steps, args.warmup, stream)
     assert st.sptp_read_device_status(ws) == 0
+    # seconds of back-to-back steps: the power-capped regime, against twice
+    # the sustained bf16 peak
+    sustained = sustained_leg(args, step, stream, dev, None, pk, 6.0 * M * d * F, 1)
+    if sustained is not None:
+        sustained["frac"] = sustained["value"] / (2.0 * pk["bf16_sustained"])
+        sustained["peak_kind"] = "2 x bf16_tflops_sustained (the nominal fp8:bf16 dense ratio)"
+        assert st.sptp_read_device_status(ws) == 0
     # the five launches of a step, each timed alone on the same buffers
     hdr = torch.zeros(st.SPTP_WS_HEADER_BYTES, dtype=torch.uint8, device=dev)
     y = torch.empty_like(T["x"])
@@ -1075,7 +1084,7 @@ def _fp8_line(args, cfg, to_dev, dev, stream, pk):
                 config={"workload": cfg.name + "_e4m3", "M": M, "d": d, "F": F, "P": P, "chunks": cfg.chunks,
                         "l2": "inputs larger than L2 (no flush)",
                         "weights": "E4M3 + row scales, quantised once outside the timed region"},
-                weight_quantisation_ms=ms_wq, kernels=kernels,
+                weight_quantisation_ms=ms_wq, kernels=kernels, sustained=sustained,
                 roofline={"bound": "tensor", "kernel": "gateup_e4m3", "achieved": gu, "peak": fp8_peak,
                           "unit": "TFLOP/s", "frac": gu / fp8_peak, "traffic": kernel_traffic("gateup_e4m3"),
                           "peak_note": "2 x measured burst bf16 (nominal fp8:bf16 dense ratio); the whole step "
