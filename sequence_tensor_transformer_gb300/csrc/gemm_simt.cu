@@ -2,21 +2,24 @@
 // cannot meet a 1e-5 relative error bound).  Same two shapes as the tcgen05
 // path: gate/up with a SwiGLU epilogue and the per-shard down projection,
 // C_g[m][n] = sum_k A_g[m][k] * B_g[n][k] with both operands K-contiguous.
-// 64 x 64 tile per CTA, 32-deep K slices staged in shared memory (the next
-// slice's loads in flight in registers while the current one is multiplied),
-// 4 x 4 outputs per thread, fp32 FMA in ascending k.
+// T x T tile per CTA (64, or 32 where 64-wide tiles would leave most SMs
+// idle), 32-deep K slices staged in shared memory (the next slice's loads in
+// flight in registers while the current one is multiplied), T/16 x T/16
+// outputs per thread, fp32 FMA in ascending k: the same arithmetic per
+// output for either tile.
 #include "sptp_internal.h"
 
 namespace sptp {
 
 namespace {
 
-constexpr int TM = 64, TN = 64, TK = 32;
-constexpr int kLoads = TM * TK / 256;  // elements of each operand a thread stages per slice
+constexpr int TK = 32;
 
-template <Epi EPI>
+template <Epi EPI, int T>
 __global__ void __launch_bounds__(256) simt_gemm_nt(const __grid_constant__ SimtGemmParams p) {
     constexpr bool SWI = EPI == Epi::kSwiGLU;
+    constexpr int TM = T, TN = T, R = T / 16;  // R x R outputs per thread
+    constexpr int kLoads = TM * TK / 256;      // elements of each operand a thread stages per slice
     __shared__ float As[TK][TM + 4];
     __shared__ float Bs0[TK][TN + 4];
     __shared__ float Bs1[SWI ? TK : 1][SWI ? TN + 4 : 1];
@@ -26,7 +29,7 @@ __global__ void __launch_bounds__(256) simt_gemm_nt(const __grid_constant__ Simt
     const float* A = p.A[g];
     const float* B0 = p.B0[g];
     const float* B1 = p.B1[g];
-    float acc0[4][4] = {}, acc1[4][4] = {};
+    float acc0[R][R] = {}, acc1[R][R] = {};
     // slice k0 of both operands into registers (zero past M, N or K)
     float ra[kLoads], rb0[kLoads], rb1[SWI ? kLoads : 1];
     auto fetch = [&](int k0) {
@@ -55,18 +58,18 @@ __global__ void __launch_bounds__(256) simt_gemm_nt(const __grid_constant__ Simt
         if (k0 + TK < p.K) fetch(k0 + TK);  // in flight during this slice's FMAs
 #pragma unroll
         for (int kk = 0; kk < TK; ++kk) {
-            float a[4], b0[4], b1[4];
+            float a[R], b0[R], b1[R];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+            for (int i = 0; i < R; ++i) a[i] = As[kk][ty * R + i];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                b0[j] = Bs0[kk][tx * 4 + j];
-                if (SWI) b1[j] = Bs1[kk][tx * 4 + j];
+            for (int j = 0; j < R; ++j) {
+                b0[j] = Bs0[kk][tx * R + j];
+                if (SWI) b1[j] = Bs1[kk][tx * R + j];
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < R; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < R; ++j) {
                     acc0[i][j] = fmaf(a[i], b0[j], acc0[i][j]);
                     if (SWI) acc1[i][j] = fmaf(a[i], b1[j], acc1[i][j]);
                 }
@@ -75,12 +78,12 @@ __global__ void __launch_bounds__(256) simt_gemm_nt(const __grid_constant__ Simt
     }
     float* C = p.C[g];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int m = m0 + ty * 4 + i;
+    for (int i = 0; i < R; ++i) {
+        const int m = m0 + ty * R + i;
         if (m >= p.M) continue;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = n0 + tx * 4 + j;
+        for (int j = 0; j < R; ++j) {
+            const int n = n0 + tx * R + j;
             if (n >= p.N) continue;
             float v = acc0[i][j];
             if (SWI) v = v / (1.0f + expf(-v)) * acc1[i][j];
@@ -93,12 +96,23 @@ __global__ void __launch_bounds__(256) simt_gemm_nt(const __grid_constant__ Simt
 
 cudaError_t launch_simt_gemm(const SimtGemmParams& p, Epi epi, cudaStream_t s) {
     if (p.M == 0 || p.N == 0 || p.G == 0) return cudaSuccess;
-    dim3 grid((p.N + TN - 1) / TN, (p.M + TM - 1) / TM, p.G);
+    // 64-wide tiles unless they would give fewer CTAs than half the SMs of
+    // this GPU (152): then 32-wide ones, four times as many
+    const long long tiles64 = static_cast<long long>((p.N + 63) / 64) * ((p.M + 63) / 64) * p.G;
+    const int T = tiles64 < 76 ? 32 : 64;
+    dim3 grid((p.N + T - 1) / T, (p.M + T - 1) / T, p.G);
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-    if (epi == Epi::kSwiGLU)
-        simt_gemm_nt<Epi::kSwiGLU><<<grid, 256, 0, s>>>(p);
-    else
-        simt_gemm_nt<Epi::kStore><<<grid, 256, 0, s>>>(p);
+    if (epi == Epi::kSwiGLU) {
+        if (T == 32)
+            simt_gemm_nt<Epi::kSwiGLU, 32><<<grid, 256, 0, s>>>(p);
+        else
+            simt_gemm_nt<Epi::kSwiGLU, 64><<<grid, 256, 0, s>>>(p);
+    } else {
+        if (T == 32)
+            simt_gemm_nt<Epi::kStore, 32><<<grid, 256, 0, s>>>(p);
+        else
+            simt_gemm_nt<Epi::kStore, 64><<<grid, 256, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 
